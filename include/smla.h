@@ -1,0 +1,217 @@
+/*
+ * smla.h -- C ABI of the GB300 paged top-k sparse-MLA library (libsmla.so).
+ *
+ * The library computes the data-parallel hot path of top-k sparse MLA over a
+ * paged FP8 KV cache held in one shared block pool:
+ *
+ *   kvpack_store       new tokens -> packed FP8 records in the pool
+ *   smla_index_scores  per-query-token indexer scores over its visible context
+ *   smla_topk          top-k cached positions per query token
+ *   smla_attend        latent MQA attention over the selected positions
+ *   smla_decode        the four steps above in one call (decode steps with
+ *                      MTP draft tokens, and chunked prefill)
+ *
+ * Sources (cited by page title and section):
+ *   [AgentX]  "vLLM、エージェント型ワークロード向け最適化技術「AgentX」を公開"
+ *             (news.ainew.jp rendering of the vLLM AgentX post), sections
+ *             "Hybrid KV cache management", "Kimi K3", "DeepSeek V4",
+ *             "Closing the loop: kernels".
+ *   [GLM-5.3] aisoku.org article on vLLM serving GLM-5.3 on 16xH200
+ *             (PCP8xDCP8 prefill, Hybrid HiSparse decode), sections
+ *             "What is new", "Config and numbers", "How to try".
+ *
+ * Conventions for every call
+ *   - All array pointers are DEVICE pointers owned by the caller; the library
+ *     never frees or retains them after the call returns.  Host pointers are
+ *     only the smla_layout_t / smla_params_t descriptors (read during the call).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = legacy default stream).  Nothing allocates device memory: scratch
+ *     space is the caller's `workspace`.
+ *   - Integer arrays are int32 unless stated; bf16 arrays are raw 16-bit
+ *     bfloat16 patterns; "e4m3" arrays are uint8 OCP FP8 E4M3 codes.
+ *   - Return value: SMLA_OK, or an error detected on the host before anything
+ *     was enqueued (SMLA_ERR_INVALID_ARG, SMLA_ERR_UNSUPPORTED) or at launch
+ *     (SMLA_ERR_CUDA).  Errors found by the kernels themselves (an out-of-range
+ *     block id or slot, a bounded wait that gave up) are latched in a device
+ *     word and reported by smla_get_last_error(); the offending read is
+ *     clamped or skipped, never performed out of bounds.
+ *   - No C++ exceptions cross the ABI.  Calls on different streams may run
+ *     concurrently; the latched error word is shared by all of them.
+ *
+ * Query geometry shared by the calls: sequence b has seq_lens[b] cached
+ * tokens INCLUDING this step's tokens, and its query tokens are rows
+ * query_start_loc[b] .. query_start_loc[b+1]-1.  Query i of the n_q tokens of
+ * sequence b sits at position p = seq_lens[b] - n_q + i and sees positions
+ * 0..p (itself included).  block_table[b * bt_stride + j / block_size] is the
+ * physical block of logical position j.
+ */
+#ifndef SMLA_H
+#define SMLA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum smla_status {
+  SMLA_OK = 0,
+  SMLA_ERR_INVALID_ARG = 1,  /* null pointer, bad size or stride          */
+  SMLA_ERR_UNSUPPORTED = 2,  /* shape not built into this library / no sm_103a device */
+  SMLA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed       */
+  SMLA_ERR_BAD_INDEX = 4,    /* device saw a block id / slot outside the pool (read clamped) */
+  SMLA_ERR_TIMEOUT = 5       /* a bounded on-device wait gave up            */
+} smla_status_t;
+
+/*
+ * Packed block-pool layout ([AgentX "Hybrid KV cache management"]: all cache
+ * groups and layers of a block in one contiguous allocation; the block is the
+ * single allocation unit).  Per block, per layer l:
+ *
+ *   [block_size latent records, rec_stride bytes each]
+ *   [block_size indexer keys, d_index e4m3 bytes each]
+ *   [block_size indexer key scales, fp32]
+ *
+ * every region on a 256-byte boundary; a record is
+ *   [d_latent e4m3 codes][d_latent/quant_tile fp32 scales][d_rope bf16] (padded to 16 B).
+ * Filled in by smla_layout_init(); read-only afterwards.
+ */
+typedef struct smla_layout {
+  int32_t block_size;     /* tokens per block                                  */
+  int32_t n_layers;       /* layers packed in one block                        */
+  int32_t d_latent;       /* latent (no-rope) dims, FP8 in the cache           */
+  int32_t d_rope;         /* rope dims, bf16 in the cache                      */
+  int32_t quant_tile;     /* latent elements per fp32 scale                    */
+  int32_t d_index;        /* indexer key dims (e4m3)                           */
+  int64_t num_blocks;     /* pool capacity in blocks                           */
+  int32_t n_scales;       /* d_latent / quant_tile                             */
+  int32_t rec_bytes;      /* d_latent + 4*n_scales + 2*d_rope                  */
+  int32_t rec_stride;     /* rec_bytes rounded up to 16                        */
+  int32_t reserved0;
+  int64_t rec_off;        /* byte offset of the record region in a layer slice */
+  int64_t idx_key_off;    /* byte offset of the indexer-key region             */
+  int64_t idx_scale_off;  /* byte offset of the indexer-scale region           */
+  int64_t layer_stride;   /* bytes of one layer slice of a block               */
+  int64_t block_stride;   /* bytes of one block (all layers)                   */
+} smla_layout_t;
+
+/* Attention / indexer hyper-parameters. */
+typedef struct smla_params {
+  int32_t n_heads;        /* query heads sharing the latent (<= 64)            */
+  int32_t n_idx_heads;    /* indexer heads                                     */
+  int32_t top_k;          /* positions kept per query token                    */
+  float softmax_scale;    /* sigma in s = sigma * (q.K + q_pe.kpe)             */
+} smla_params_t;
+
+/* Fill `layout` from the shape; checks divisibility.  Host only, no device work. */
+smla_status_t smla_layout_init(smla_layout_t* layout, int block_size, int n_layers, int d_latent,
+                               int d_rope, int quant_tile, int d_index, int64_t num_blocks);
+
+/* Bytes of `workspace` that smla_decode needs for these sizes (scores + top-k
+ * scratch, 256-byte aligned pieces).  max_ctx = the largest seq_lens entry. */
+size_t smla_workspace_size(const smla_layout_t* layout, const smla_params_t* params,
+                           int n_tokens, int max_ctx);
+
+/*
+ * kvpack_store -- write n_tokens new tokens into layer `layer` of the pool.
+ * [GLM-5.3 "How to try", "Config and numbers"]: the KV cache is FP8.
+ *   latent      bf16 [n_tokens, d_latent]
+ *   rope        bf16 [n_tokens, d_rope]
+ *   idx_k       e4m3 [n_tokens, d_index]   copied verbatim
+ *   idx_scale   fp32 [n_tokens]            copied verbatim
+ *   slot_mapping int64 [n_tokens]          physical slot (block*block_size+off); -1 = skip
+ * Per quant_tile of the latent: scale = amax/448 (IEEE fp32 division; 1.0 if
+ * that is 0), code = E4M3 round-to-nearest-even, saturating, of x/scale.
+ * Latent values must be finite.  Slots >= num_blocks*block_size are skipped
+ * and latch SMLA_ERR_BAD_INDEX.
+ */
+smla_status_t kvpack_store(const smla_layout_t* layout, void* pool, int layer, const void* latent,
+                           const void* rope, const uint8_t* idx_k, const float* idx_scale,
+                           const int64_t* slot_mapping, int n_tokens, void* stream);
+
+/*
+ * smla_index_scores -- indexer scores of every query token over its context.
+ * [AgentX "DeepSeek V4"]: 64 indexer heads produce one global selection per
+ * token; [GLM-5.3 "What is new"]: the indexer cost is quadratic in context.
+ *   I[t, j] = s_I[j] * sum_h w[t, h] * ReLU(sum_d q_idx[t, h, d] * k_I[j, d]),  j <= p(t)
+ * computed with FP8 tensor-core MMAs, fp32 accumulation and an fp32 head
+ * reduction in head order.
+ *   q_idx   e4m3 [n_tokens, n_idx_heads, d_index]
+ *   w       fp32 [n_tokens, n_idx_heads]
+ *   scores  fp32 [n_tokens, scores_stride]: entries j <= p(t) are written,
+ *           the rest of each row is left untouched.  scores_stride >= max_ctx.
+ *   max_q   largest number of query tokens of one sequence in this call
+ *   max_ctx largest seq_lens entry
+ */
+smla_status_t smla_index_scores(const smla_layout_t* layout, const smla_params_t* params,
+                                const void* pool, int layer, const uint8_t* q_idx, const float* w,
+                                const int32_t* block_table, int bt_stride, const int32_t* seq_lens,
+                                const int32_t* query_start_loc, int batch, int n_tokens, int max_q,
+                                int max_ctx, float* scores, int64_t scores_stride, void* stream);
+
+/*
+ * smla_topk -- exact top-k of each row of `scores` over positions 0..p(t).
+ * [GLM-5.3 "What is new"] (2,048 tokens), [AgentX "DeepSeek V4"].
+ * Ties go to the lower position; scores compare as fp32 values (-0 == +0).
+ *   topk_idx int32 [n_tokens, top_k]: kept logical positions in ascending
+ *            order, -1 padded when p(t)+1 < top_k.
+ */
+smla_status_t smla_topk(const smla_params_t* params, const float* scores, int64_t scores_stride,
+                        const int32_t* seq_lens, const int32_t* query_start_loc, int batch,
+                        int n_tokens, int32_t* topk_idx, void* stream);
+
+/*
+ * smla_attend -- latent MQA attention over the selected positions.
+ * [AgentX "Kimi K3"], [GLM-5.3 "What is new"]: the latent KV is shared by
+ * all query heads; [AgentX "DeepSeek V4"]: attention runs over the top-k only.
+ *   s[h, j] = softmax_scale * (q[t, h] . K[j] + q_pe[t, h] . kpe[j]),
+ *   out[t, h] = sum_j softmax_j(s)[h, j] * K[j],  lse[t, h] = ln sum_j exp(s[h, j])
+ * with K[j] the dequantised latent and kpe[j] the cached rope.
+ *   q        bf16 [n_tokens, n_heads, d_latent]
+ *   q_pe     bf16 [n_tokens, n_heads, d_rope]
+ *   topk_idx int32 [n_tokens, top_k]; entries < 0 are ignored
+ *   out      bf16 [n_tokens, n_heads, d_latent]
+ *   lse      fp32 [n_tokens, n_heads]  (natural log; -inf and out = 0 when no entry is valid)
+ */
+smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* params, const void* pool,
+                          int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
+                          const int32_t* block_table, int bt_stride, const int32_t* query_start_loc,
+                          int batch, int n_tokens, void* out, float* lse, void* stream);
+
+/*
+ * smla_decode -- one step of the whole path for one layer:
+ * kvpack_store(new tokens) -> smla_index_scores -> smla_topk -> smla_attend.
+ * Serves decode steps with MTP drafts ([GLM-5.3 "Config and numbers"]: MTP3)
+ * and chunked prefill on a cached prefix (many query tokens per sequence).
+ *   new_latent/new_rope/new_idx_k/new_idx_scale/slot_mapping: as kvpack_store,
+ *     n_tokens rows (slot_mapping may be NULL to skip the store)
+ *   topk_idx_out: optional int32 [n_tokens, top_k] copy of the selection (NULL = none)
+ *   workspace: device scratch of at least smla_workspace_size(...) bytes,
+ *     256-byte aligned
+ * Query tokens are processed in groups so the score scratch stays bounded.
+ */
+smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* params, void* pool,
+                          int layer, const void* new_latent, const void* new_rope,
+                          const uint8_t* new_idx_k, const float* new_idx_scale,
+                          const int64_t* slot_mapping, const void* q, const void* q_pe,
+                          const uint8_t* q_idx, const float* w, const int32_t* block_table,
+                          int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                          int batch, int n_tokens, int max_q, int max_ctx, void* out, float* lse,
+                          int32_t* topk_idx_out, void* workspace, size_t workspace_bytes,
+                          void* stream);
+
+/* Synchronise `stream`, return the latched device error (and clear it). */
+smla_status_t smla_get_last_error(void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* smla_status_string(smla_status_t status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int smla_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SMLA_H */

@@ -1,0 +1,203 @@
+"""Python binding of libsmla, the GB300 paged top-k sparse-MLA library.
+
+Argument marshalling only: every function takes torch CUDA tensors, checks
+dtypes and shapes, and calls the same-named C entry point of
+``include/smla.h`` through ctypes.  All computation happens in the library's
+CUDA kernels; there is no CPU path.  If ``_build/libsmla.so`` is missing the
+import of ``lib()`` raises -- build it with ``paged_sparse_mla_gb300.build_lib.build()``.
+"""
+
+import ctypes
+import os
+
+import torch
+
+from . import build_lib
+
+__all__ = [
+    "SmlaError", "Layout", "Params", "lib", "layout_init", "workspace_size", "kvpack_store",
+    "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
+    "status_string", "version", "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = (
+    "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
+    "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
+)
+
+STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
+          4: "SMLA_ERR_BAD_INDEX", 5: "SMLA_ERR_TIMEOUT"}
+
+
+class SmlaError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {STATUS.get(code, code)}")
+
+
+class Layout(ctypes.Structure):
+    """Mirror of smla_layout_t."""
+    _fields_ = [
+        ("block_size", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("d_latent", ctypes.c_int32),
+        ("d_rope", ctypes.c_int32), ("quant_tile", ctypes.c_int32), ("d_index", ctypes.c_int32),
+        ("num_blocks", ctypes.c_int64), ("n_scales", ctypes.c_int32), ("rec_bytes", ctypes.c_int32),
+        ("rec_stride", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("rec_off", ctypes.c_int64),
+        ("idx_key_off", ctypes.c_int64), ("idx_scale_off", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
+        ("block_stride", ctypes.c_int64),
+    ]
+
+    @property
+    def pool_bytes(self) -> int:
+        return self.num_blocks * self.block_stride
+
+
+class Params(ctypes.Structure):
+    """Mirror of smla_params_t."""
+    _fields_ = [("n_heads", ctypes.c_int32), ("n_idx_heads", ctypes.c_int32), ("top_k", ctypes.c_int32),
+                ("softmax_scale", ctypes.c_float)]
+
+
+_LIB = None
+_P = ctypes.c_void_p
+_I = ctypes.c_int
+_I64 = ctypes.c_int64
+
+
+def lib() -> ctypes.CDLL:
+    """Load libsmla.so (built in-tree).  Raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(build_lib.LIB):
+            raise RuntimeError(f"libsmla.so not built ({build_lib.LIB}); run paged_sparse_mla_gb300.build_lib.build()")
+        L = ctypes.CDLL(build_lib.LIB)
+        LP, PP = ctypes.POINTER(Layout), ctypes.POINTER(Params)
+        sig = {
+            "smla_layout_init": (_I, [LP, _I, _I, _I, _I, _I, _I, _I64]),
+            "smla_workspace_size": (ctypes.c_size_t, [LP, PP, _I, _I]),
+            "kvpack_store": (_I, [LP, _P, _I, _P, _P, _P, _P, _P, _I, _P]),
+            "smla_index_scores": (_I, [LP, PP, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _I64, _P]),
+            "smla_topk": (_I, [PP, _P, _I64, _P, _P, _I, _I, _P, _P]),
+            "smla_attend": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P]),
+            "smla_decode": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I,
+                                 _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "smla_get_last_error": (_I, [_P]),
+            "smla_status_string": (ctypes.c_char_p, [_I]),
+            "smla_version": (_I, []),
+        }
+        for name, (res, args) in sig.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(code: int, where: str) -> None:
+    if code != 0:
+        raise SmlaError(code, where)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("libsmla takes CUDA tensors only")
+    if not t.is_contiguous():
+        raise ValueError("libsmla takes contiguous tensors only")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _expect(t, dtype, name):
+    if t.dtype != dtype:
+        raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def version() -> int:
+    return lib().smla_version()
+
+
+def status_string(code: int) -> str:
+    return lib().smla_status_string(code).decode()
+
+
+def layout_init(block_size, n_layers, d_latent, d_rope, quant_tile, d_index, num_blocks) -> Layout:
+    lay = Layout()
+    _check(lib().smla_layout_init(ctypes.byref(lay), block_size, n_layers, d_latent, d_rope, quant_tile, d_index,
+                                  num_blocks), "smla_layout_init")
+    return lay
+
+
+def make_params(n_heads, n_idx_heads, top_k, softmax_scale) -> Params:
+    return Params(n_heads, n_idx_heads, top_k, softmax_scale)
+
+
+def workspace_size(layout: Layout, params: Params, n_tokens: int, max_ctx: int) -> int:
+    return int(lib().smla_workspace_size(ctypes.byref(layout), ctypes.byref(params), n_tokens, max_ctx))
+
+
+def kvpack_store(layout, pool, layer, latent, rope, idx_k, idx_scale, slot_mapping, stream=None):
+    _expect(pool, torch.uint8, "pool")
+    _expect(latent, torch.bfloat16, "latent")
+    _expect(rope, torch.bfloat16, "rope")
+    _expect(idx_k, torch.uint8, "idx_k")
+    _expect(idx_scale, torch.float32, "idx_scale")
+    _expect(slot_mapping, torch.int64, "slot_mapping")
+    n = slot_mapping.numel()
+    _check(lib().kvpack_store(ctypes.byref(layout), _ptr(pool), layer, _ptr(latent), _ptr(rope), _ptr(idx_k),
+                              _ptr(idx_scale), _ptr(slot_mapping), n, _stream(stream)), "kvpack_store")
+
+
+def smla_index_scores(layout, params, pool, layer, q_idx, w, block_table, seq_lens, query_start_loc, max_q,
+                      max_ctx, scores, stream=None):
+    _expect(q_idx, torch.uint8, "q_idx")
+    _expect(w, torch.float32, "w")
+    _expect(block_table, torch.int32, "block_table")
+    _expect(scores, torch.float32, "scores")
+    n_tokens = q_idx.shape[0]
+    _check(lib().smla_index_scores(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(q_idx),
+                                   _ptr(w), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
+                                   _ptr(query_start_loc), seq_lens.numel(), n_tokens, max_q, max_ctx, _ptr(scores),
+                                   scores.stride(0), _stream(stream)), "smla_index_scores")
+
+
+def smla_topk(params, scores, seq_lens, query_start_loc, topk_idx, stream=None):
+    _expect(scores, torch.float32, "scores")
+    _expect(topk_idx, torch.int32, "topk_idx")
+    _check(lib().smla_topk(ctypes.byref(params), _ptr(scores), scores.stride(0), _ptr(seq_lens),
+                           _ptr(query_start_loc), seq_lens.numel(), topk_idx.shape[0], _ptr(topk_idx),
+                           _stream(stream)), "smla_topk")
+
+
+def smla_attend(layout, params, pool, layer, q, q_pe, topk_idx, block_table, query_start_loc, out, lse,
+                stream=None):
+    _expect(q, torch.bfloat16, "q")
+    _expect(q_pe, torch.bfloat16, "q_pe")
+    _expect(out, torch.bfloat16, "out")
+    _expect(lse, torch.float32, "lse")
+    _check(lib().smla_attend(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(q), _ptr(q_pe),
+                             _ptr(topk_idx), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
+                             query_start_loc.numel() - 1, q.shape[0], _ptr(out), _ptr(lse), _stream(stream)),
+           "smla_attend")
+
+
+def smla_decode(layout, params, pool, layer, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping, q, q_pe,
+                q_idx, w, block_table, seq_lens, query_start_loc, max_q, max_ctx, out, lse, workspace,
+                topk_idx_out=None, stream=None):
+    _expect(q, torch.bfloat16, "q")
+    _expect(workspace, torch.uint8, "workspace")
+    _check(lib().smla_decode(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(new_latent),
+                             _ptr(new_rope), _ptr(new_idx_k), _ptr(new_idx_scale), _ptr(slot_mapping), _ptr(q),
+                             _ptr(q_pe), _ptr(q_idx), _ptr(w), _ptr(block_table), block_table.shape[1],
+                             _ptr(seq_lens), _ptr(query_start_loc), seq_lens.numel(), q.shape[0], max_q, max_ctx,
+                             _ptr(out), _ptr(lse), _ptr(topk_idx_out), _ptr(workspace), workspace.numel(),
+                             _stream(stream)), "smla_decode")
+
+
+def smla_get_last_error(stream=None) -> int:
+    return int(lib().smla_get_last_error(_stream(stream)))

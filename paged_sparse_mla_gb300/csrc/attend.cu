@@ -1,0 +1,544 @@
+// smla_attend: latent MQA attention of each query token over its top-k positions.
+//
+// [AgentX "Kimi K3"], [GLM-5.3 "What is new"]: MLA keeps one latent KV shared
+// by all 64 query heads, so attention is MQA over the latent; V is the latent.
+// [AgentX "DeepSeek V4"]: sparse MLA attends only over the top-k entries, and
+// gathering them dominates.  [AgentX "Kimi K3"] (DCP): the output carries
+// log-sum-exp statistics so partial results can be merged.
+//
+// Design (sm_103a, one persistent CTA per SM, one query token at a time):
+//   * 128 selected positions form a tile.  Producer warps (4-6) translate the
+//     logical positions through the block table, read the 656-byte records
+//     (L2 prefetch of the next tile with cp.async.bulk.prefetch), dequantise the
+//     E4M3 latent with its per-128 fp32 scales to bf16, and write the tile as
+//     9 chunks of [128 keys x 64 dims] with the 128-byte swizzle (8 latent
+//     chunks + 1 rope chunk); the query is staged the same way (64 heads).
+//   * MMA1 (warp 7): S^T[key, head] = Khat[key, :] . q[head, :] over 576 dims,
+//     M = 128 keys, N = 64 heads, fp32 in tensor memory.  TMEM lane = key.
+//   * Softmax (warps 0-3, thread = key): per-head tile maxima with a butterfly
+//     transpose-reduction across lanes, online softmax with lazy rescaling
+//     (the running max only moves when a head's tile max exceeds it by 2^8),
+//     P^T[key, head] written as bf16 into the rope chunk (free after MMA1),
+//     per-thread partial row sums.
+//   * MMA2: O^T[dim, head] += V^T[dim, key] . P^T[key, head] with both operands
+//     MN-major: the same swizzled latent chunks serve as V^T without a
+//     transpose; M = 128 dims x 4 tiles, N = 64 heads, K = 128 keys.
+//   * Epilogue: O^T / l -> bf16 out[t, h, d] (thread = dim, coalesced) and
+//     lse = ln(sum) from the running max and the reduced row sums.
+#include "smla_internal.h"
+
+namespace smla {
+namespace {
+
+constexpr int kTile = 128;     // keys per tile
+constexpr int kHeads = 64;     // MMA N: query heads (zero padded)
+constexpr int kProducerThreads = 96;               // warps 4-6
+constexpr int kMmaWarp = 7;
+constexpr int kThreads = 32 * 8;
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.6931471805599453f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+template <int NCH>
+struct __align__(1024) AttnSmem {
+  uint8_t kv[NCH][kTile * 128];    // chunk c: [128 keys][64 dims] bf16, swizzled; chunk NCH-1: rope, then P^T
+  uint8_t q[NCH][kHeads * 128];    // chunk c: [64 heads][64 dims] bf16, swizzled
+  const uint8_t* rec[kTile];       // record address per key of the tile being gathered (nullptr = masked)
+  float red[4][kHeads];
+  float m_tile[kHeads];
+  float m_run[kHeads];
+  float alpha[kHeads];
+  float l_fin[kHeads];
+  int ntiles[2];
+  uint64_t tok_full[2], tok_empty[2];
+  uint64_t q_full, q_empty, kv_full, kv_empty, s_full, p_full, o_done, final_bar;
+  uint32_t tmem_slot;
+  int abort;
+  int rescale;
+};
+
+struct AttnArgs {
+  KernelLayout L;
+  int n_heads, top_k, layer;
+  float scale_log2;  // softmax_scale * log2(e)
+  const uint8_t* pool;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* q_pe;
+  const int32_t* topk;  // rows relative to tok_begin
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t* qsl;
+  int batch, tok_begin, n_rows;
+  __nv_bfloat16* out;
+  float* lse;
+  unsigned* err;
+};
+
+// Transpose-reduce 64 per-lane values across the 32 lanes of a warp: afterwards
+// lane l holds the reduction of heads 2l and 2l+1 in v[0], v[1].
+template <bool kMax>
+__device__ __forceinline__ void warp_transpose_reduce(float (&v)[kHeads], int lane) {
+#pragma unroll
+  for (int st = 0; st < 5; ++st) {
+    const int off = 16 >> st;
+    const int half = 32 >> st;
+    const bool upper = (lane & off) != 0;
+#pragma unroll
+    for (int i = 0; i < half; ++i) {
+      const float send = upper ? v[i] : v[i + half];
+      const float keep = upper ? v[i + half] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, off);
+      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+}
+
+// Eight bf16 values from 2-byte aligned memory; entries at or beyond `avail` read as zero.
+__device__ __forceinline__ uint4 load_bf16x8_padded(const uint16_t* src, int avail) {
+  uint32_t w[4];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const uint32_t lo = (2 * x < avail) ? src[2 * x] : 0u;
+    const uint32_t hi = (2 * x + 1 < avail) ? src[2 * x + 1] : 0u;
+    w[x] = lo | (hi << 16);
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Number of 128-key tiles a row needs: one past the last valid entry.
+__device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
+  int last = -1;
+  for (int i = lane; i < k; i += 32)
+    if (__ldg(row + i) >= 0) last = i;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
+  return (last + kTile) / kTile;
+}
+
+template <int NCH>
+__global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
+  extern __shared__ uint8_t smem_raw[];
+  AttnSmem<NCH>& sm =
+      *reinterpret_cast<AttnSmem<NCH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kLatChunks = NCH - 1;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const KernelLayout& L = A.L;
+  const int DL = L.d_latent, DR = L.d_rope;
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sm.tok_full[i], 1);
+      mbar_init(&sm.tok_empty[i], 5);
+    }
+    mbar_init(&sm.q_full, kProducerThreads);
+    mbar_init(&sm.q_empty, 1);
+    mbar_init(&sm.kv_full, kProducerThreads);
+    mbar_init(&sm.kv_empty, 1);
+    mbar_init(&sm.s_full, 1);
+    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.o_done, 1);
+    mbar_init(&sm.final_bar, 1);
+    sm.abort = 0;
+    mbar_fence_init();
+  }
+  if (warp == kMmaWarp) tmem_alloc(&sm.tmem_slot, 512);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem_slot;
+  const uint32_t tmem_o = tmem;         // O^T: 4 d-tiles x 64 columns
+  const uint32_t tmem_s = tmem + 256;   // S^T: 64 columns
+  volatile int* abort = &sm.abort;
+
+  if (warp >= 4 && warp < kMmaWarp) {
+    // ------------------------------ producers ------------------------------
+    const int ptid = threadIdx.x - 128;  // 0..95
+    uint32_t n = 0, nw = 0, kk = 0;
+    const int parts = DL / 16;           // 16-code parts per record
+    const bool rope16 = ((DL + 4 * L.n_scales) % 16) == 0;
+    for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
+      const int t = A.tok_begin + tr;
+      const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
+      const int ntiles = row_tiles(idx, A.top_k, lane);
+      if (warp == 4 && lane == 0) {
+        if (!mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) break;
+        sm.ntiles[n & 1] = ntiles;
+        mbar_arrive(&sm.tok_full[n & 1]);
+      }
+      if (ntiles == 0) continue;
+      const int b = seq_of_token(A.qsl, A.batch, t);
+      const int32_t* bt = A.block_table + static_cast<int64_t>(b) * A.bt_stride;
+      // ---- query -> swizzled bf16 chunks (heads and rope dims zero padded) ----
+      if (!mbar_wait(&sm.q_empty, (nw & 1) ^ 1, A.err, abort)) break;
+      for (int u = ptid; u < kHeads * NCH * 8; u += kProducerThreads) {
+        const int h = u / (NCH * 8), rem = u % (NCH * 8), c = rem / 8, v = rem % 8;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if (h < A.n_heads) {
+          if (c < kLatChunks) {
+            val = __ldg(reinterpret_cast<const uint4*>(A.q + (static_cast<int64_t>(t) * A.n_heads + h) * DL + c * 64) + v);
+          } else if (v * 8 < DR) {
+            const uint16_t* src =
+                reinterpret_cast<const uint16_t*>(A.q_pe + (static_cast<int64_t>(t) * A.n_heads + h) * DR) + v * 8;
+            val = load_bf16x8_padded(src, DR - v * 8);
+          }
+        }
+        *reinterpret_cast<uint4*>(&sm.q[c][sw128_off(h, v)]) = val;
+      }
+      fence_proxy_async();
+      mbar_arrive(&sm.q_full);
+      // ---- key tiles ----
+      bool ok = true;
+      for (int tile = 0; tile < ntiles; ++tile, ++kk) {
+        if (!mbar_wait(&sm.kv_empty, (kk & 1) ^ 1, A.err, abort)) {
+          ok = false;
+          break;
+        }
+        named_bar_sync(2, kProducerThreads);  // previous tile's rec[] fully consumed
+        for (int rr = ptid; rr < kTile; rr += kProducerThreads) {
+          const int e = tile * kTile + rr;
+          const int j = e < A.top_k ? __ldg(idx + e) : -1;
+          const uint8_t* r = nullptr;
+          if (j >= 0) {
+            const int blk = __ldg(bt + j / L.block_size);
+            if (blk < 0 || blk >= L.num_blocks) {
+              latch_error(A.err, SMLA_ERR_BAD_INDEX);
+            } else {
+              r = A.pool + static_cast<int64_t>(blk) * L.block_stride + static_cast<int64_t>(A.layer) * L.layer_stride +
+                  L.rec_off + static_cast<int64_t>(j % L.block_size) * L.rec_stride;
+            }
+          }
+          sm.rec[rr] = r;
+          // warm L2 with the next tile's record
+          const int e2 = e + kTile;
+          if (e2 < A.top_k) {
+            const int j2 = __ldg(idx + e2);
+            if (j2 >= 0) {
+              const int blk2 = __ldg(bt + j2 / L.block_size);
+              if (blk2 >= 0 && blk2 < L.num_blocks)
+                prefetch_l2_bulk(A.pool + static_cast<int64_t>(blk2) * L.block_stride +
+                                     static_cast<int64_t>(A.layer) * L.layer_stride + L.rec_off +
+                                     static_cast<int64_t>(j2 % L.block_size) * L.rec_stride,
+                                 static_cast<uint32_t>(L.rec_stride));
+            }
+          }
+        }
+        named_bar_sync(2, kProducerThreads);
+        // latent: 16 E4M3 codes -> 16 bf16 (two 16-byte units) per step
+        for (int u = ptid; u < kTile * parts; u += kProducerThreads) {
+          const int r = u / parts, part = u % parts;
+          const uint8_t* rec = sm.rec[r];
+          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
+          if (rec != nullptr) {
+            const uint4 codes = __ldg(reinterpret_cast<const uint4*>(rec) + part);
+            const float sc = __ldg(reinterpret_cast<const float*>(rec + DL) + (part * 16) / L.quant_tile);
+            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+            uint32_t ow[8];
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+              const __half2_raw h01 =
+                  __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] & 0xFFFFu), __NV_E4M3);
+              const __half2_raw h23 =
+                  __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] >> 16), __NV_E4M3);
+              const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+              const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+              ow[2 * x] = pack_bf16x2(f01.x * sc, f01.y * sc);
+              ow[2 * x + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
+            }
+            o0 = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+            o1 = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+          }
+          const int d0 = part * 16;
+          const int c = d0 / 64, v0 = (d0 % 64) / 8;
+          *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0)]) = o0;
+          *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0 + 1)]) = o1;
+        }
+        // rope (bf16) copied into the last chunk, zero padded to 64 dims
+        for (int u = ptid; u < kTile * 8; u += kProducerThreads) {
+          const int r = u / 8, v = u % 8;
+          const uint8_t* rec = sm.rec[r];
+          uint4 val = make_uint4(0, 0, 0, 0);
+          if (rec != nullptr && v * 8 < DR) {
+            const uint8_t* src = rec + DL + 4 * L.n_scales + v * 16;
+            if (rope16 && v * 8 + 8 <= DR) {
+              val = __ldg(reinterpret_cast<const uint4*>(src));
+            } else {
+              val = load_bf16x8_padded(reinterpret_cast<const uint16_t*>(src), DR - v * 8);
+            }
+          }
+          *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(r, v)]) = val;
+        }
+        fence_proxy_async();
+        mbar_arrive(&sm.kv_full);
+      }
+      if (!ok) break;
+      ++nw;
+    }
+  } else if (warp == kMmaWarp) {
+    // ------------------------------ MMA issuer ------------------------------
+    if (lane == 0) {
+      uint32_t n = 0, nw = 0, kk = 0;
+      bool issued = false;
+      const uint32_t idesc1 = make_idesc(128, kHeads, 1, 1, 0, 0);  // bf16, both K-major
+      const uint32_t idesc2 = make_idesc(128, kHeads, 1, 1, 1, 1);  // bf16, both MN-major
+      const int dtiles = (DL + 127) / 128;
+      const uint32_t kv0 = smem_u32(sm.kv[0]);
+      const uint32_t q0 = smem_u32(sm.q[0]);
+      const uint32_t pt = smem_u32(sm.kv[kLatChunks]);
+      for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
+        if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
+        const int ntiles = sm.ntiles[n & 1];
+        mbar_arrive(&sm.tok_empty[n & 1]);
+        if (ntiles == 0) continue;
+        if (!mbar_wait(&sm.q_full, nw & 1, A.err, abort)) break;
+        bool ok = true;
+        for (int tile = 0; tile < ntiles; ++tile, ++kk) {
+          if (!mbar_wait(&sm.kv_full, kk & 1, A.err, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int c = 0; c < NCH; ++c) {
+            for (int k4 = 0; k4 < 4; ++k4) {
+              mma_f16(tmem_s, sw128_desc(kv0 + c * kTile * 128 + k4 * 32, 16, 1024),
+                      sw128_desc(q0 + c * kHeads * 128 + k4 * 32, 16, 1024), idesc1, (c | k4) != 0);
+            }
+          }
+          issued = true;
+          mma_commit(&sm.s_full);
+          if (tile == ntiles - 1) mma_commit(&sm.q_empty);
+          if (!mbar_wait(&sm.p_full, kk & 1, A.err, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          for (int d2 = 0; d2 < dtiles; ++d2) {
+            for (int k8 = 0; k8 < kTile / 16; ++k8) {
+              mma_f16(tmem_o + d2 * kHeads, sw128_desc(kv0 + 2 * d2 * kTile * 128 + k8 * 2048, kTile * 128, 1024),
+                      sw128_desc(pt + k8 * 2048, kTile * 128, 1024), idesc2, (tile | k8) != 0);
+            }
+          }
+          mma_commit(&sm.kv_empty);
+          if (tile == ntiles - 1) mma_commit(&sm.o_done);
+        }
+        if (!ok) break;
+        ++nw;
+      }
+      if (issued) {
+        mma_commit(&sm.final_bar);
+        mbar_wait(&sm.final_bar, 0, A.err, abort);
+      }
+    }
+  } else {
+    // ------------------------------ softmax + epilogue (warps 0-3) ------------------------------
+    const int tid = threadIdx.x;  // key row of the tile / dim row of an O^T tile
+    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    uint32_t n = 0, nw = 0, kk = 0;
+    for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
+      const int t = A.tok_begin + tr;
+      if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
+      const int ntiles = sm.ntiles[n & 1];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.tok_empty[n & 1]);
+      if (ntiles == 0) {
+        for (int i = tid; i < A.n_heads * DL; i += 128)
+          A.out[static_cast<int64_t>(t) * A.n_heads * DL + i] = __float2bfloat16(0.f);
+        if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = -INFINITY;
+        continue;
+      }
+      const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
+      float l_part[kHeads];
+#pragma unroll
+      for (int h = 0; h < kHeads; ++h) l_part[h] = 0.f;
+      bool ok = true;
+      for (int tile = 0; tile < ntiles; ++tile, ++kk) {
+        const int e = tile * kTile + tid;
+        const bool valid = e < A.top_k && __ldg(idx + e) >= 0;
+        if (!mbar_wait(&sm.s_full, kk & 1, A.err, abort)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // per-head maximum of this tile
+        {
+          float v[kHeads];
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            uint32_t r[32];
+            tmem_ld32(tmem_s + lane_base + 32 * half, r);
+            tmem_ld_wait();
+#pragma unroll
+            for (int h = 0; h < 32; ++h) v[32 * half + h] = valid ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
+          }
+          warp_transpose_reduce<true>(v, lane);
+          sm.red[warp][2 * lane] = v[0];
+          sm.red[warp][2 * lane + 1] = v[1];
+        }
+        named_bar_sync(1, 128);
+        if (tid < kHeads) {
+          const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
+          sm.m_tile[tid] = mt;
+        }
+        named_bar_sync(1, 128);
+        if (tid == 0) {
+          int need = 0;
+          if (tile == 0) {
+            need = 1;
+          } else {
+            for (int h = 0; h < kHeads; ++h) need |= sm.m_tile[h] > sm.m_run[h] + kRescaleThreshold;
+          }
+          sm.rescale = need;
+        }
+        named_bar_sync(1, 128);
+        if (sm.rescale) {
+          if (tid < kHeads) {
+            const float old = tile == 0 ? -INFINITY : sm.m_run[tid];
+            const float mn = fmaxf(old, sm.m_tile[tid]);
+            sm.alpha[tid] = (tile == 0 || mn == -INFINITY) ? 1.f : exp2f(old - mn);
+            sm.m_run[tid] = mn;
+          }
+          named_bar_sync(1, 128);
+          if (tile > 0) {
+#pragma unroll
+            for (int h = 0; h < kHeads; ++h) l_part[h] *= sm.alpha[h];
+            const int dtiles = (DL + 127) / 128;
+            for (int d2 = 0; d2 < dtiles; ++d2) {
+              for (int hh = 0; hh < kHeads; hh += 32) {
+                uint32_t o[32];
+                tmem_ld32(tmem_o + lane_base + d2 * kHeads + hh, o);
+                tmem_ld_wait();
+#pragma unroll
+                for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * sm.alpha[hh + x]);
+                tmem_st32(tmem_o + lane_base + d2 * kHeads + hh, o);
+              }
+            }
+            tmem_st_wait();
+          }
+        }
+        // probabilities -> bf16 P^T row (this key) in the rope chunk
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+          uint32_t r[32];
+          tmem_ld32(tmem_s + lane_base + 32 * half, r);
+          tmem_ld_wait();
+          uint32_t pw[16];
+#pragma unroll
+          for (int hx = 0; hx < 32; hx += 2) {
+            const int h = 32 * half + hx;
+            const float m0 = sm.m_run[h], m1 = sm.m_run[h + 1];
+            const float s0 = valid ? __uint_as_float(r[hx]) * A.scale_log2 : -INFINITY;
+            const float s1 = valid ? __uint_as_float(r[hx + 1]) * A.scale_log2 : -INFINITY;
+            const float p0 = exp2f(s0 - (m0 == -INFINITY ? 0.f : m0));
+            const float p1 = exp2f(s1 - (m1 == -INFINITY ? 0.f : m1));
+            const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
+            const float2 pf = __bfloat1622float2(pb);
+            l_part[h] += pf.x;
+            l_part[h + 1] += pf.y;
+            pw[hx / 2] = (static_cast<uint32_t>(__bfloat16_as_ushort(pb.y)) << 16) | __bfloat16_as_ushort(pb.x);
+          }
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(tid, 4 * half + v)]) =
+                make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+          }
+        }
+        fence_proxy_async();
+        tc_fence_before();
+        mbar_arrive(&sm.p_full);
+      }
+      if (!ok) break;
+      // ---- end of token: row sums, normalisation, lse ----
+      if (!mbar_wait(&sm.o_done, nw & 1, A.err, abort)) break;
+      tc_fence_after();
+      warp_transpose_reduce<false>(l_part, lane);
+      sm.red[warp][2 * lane] = l_part[0];
+      sm.red[warp][2 * lane + 1] = l_part[1];
+      named_bar_sync(1, 128);
+      if (tid < kHeads) {
+        const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
+        sm.l_fin[tid] = l;
+        if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = (sm.m_run[tid] + log2f(l)) * kLn2;
+      }
+      named_bar_sync(1, 128);
+      const int dtiles = (DL + 127) / 128;
+      for (int d2 = 0; d2 < dtiles; ++d2) {
+        const int d = d2 * 128 + tid;
+        for (int hh = 0; hh < kHeads; hh += 32) {
+          uint32_t o[32];
+          tmem_ld32(tmem_o + lane_base + d2 * kHeads + hh, o);
+          tmem_ld_wait();
+          if (d < DL) {
+#pragma unroll
+            for (int x = 0; x < 32; ++x) {
+              const int h = hh + x;
+              if (h < A.n_heads)
+                A.out[(static_cast<int64_t>(t) * A.n_heads + h) * DL + d] =
+                    __float2bfloat16(__uint_as_float(o[x]) / sm.l_fin[h]);
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      named_bar_sync(1, 128);  // l_fin / m_run reused by the next token
+      ++nw;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+template <int NCH>
+smla_status_t launch_nch(const AttnArgs& A, cudaStream_t stream) {
+  const size_t smem = sizeof(AttnSmem<NCH>) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(attend_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    attr_set = true;
+  }
+  const int grid = min(A.n_rows, device_sm_count());
+  attend_kernel<NCH><<<grid, kThreads, smem, stream>>>(A);
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+}
+
+}  // namespace
+
+smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float softmax_scale, const void* pool,
+                            int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
+                            const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
+                            int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err) {
+  if (tok_end <= tok_begin) return SMLA_OK;
+  if (n_heads > kHeads || L.d_rope > 64 || L.d_latent % 64 != 0) return SMLA_ERR_UNSUPPORTED;
+  AttnArgs A;
+  A.L = L;
+  A.n_heads = n_heads;
+  A.top_k = top_k;
+  A.layer = layer;
+  A.scale_log2 = softmax_scale * kLog2e;
+  A.pool = static_cast<const uint8_t*>(pool);
+  A.q = static_cast<const __nv_bfloat16*>(q);
+  A.q_pe = static_cast<const __nv_bfloat16*>(q_pe);
+  A.topk = topk_idx;
+  A.block_table = block_table;
+  A.bt_stride = bt_stride;
+  A.qsl = query_start_loc;
+  A.batch = batch;
+  A.tok_begin = tok_begin;
+  A.n_rows = tok_end - tok_begin;
+  A.out = static_cast<__nv_bfloat16*>(out);
+  A.lse = lse;
+  A.err = err;
+  switch (L.d_latent / 64) {
+    case 1: return launch_nch<2>(A, stream);
+    case 8: return launch_nch<9>(A, stream);
+    default: return SMLA_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace smla

@@ -1,0 +1,60 @@
+// Internal declarations shared by the libsmla translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "smla.h"
+#include "smla_device.cuh"
+
+namespace smla {
+
+// Kernel-side copy of smla_layout_t (passed by value).
+struct KernelLayout {
+  int32_t block_size, n_layers, d_latent, d_rope, quant_tile, d_index, n_scales, rec_stride;
+  int64_t num_blocks, rec_off, idx_key_off, idx_scale_off, layer_stride, block_stride;
+};
+
+inline KernelLayout kernel_layout(const smla_layout_t& l) {
+  KernelLayout k;
+  k.block_size = l.block_size;
+  k.n_layers = l.n_layers;
+  k.d_latent = l.d_latent;
+  k.d_rope = l.d_rope;
+  k.quant_tile = l.quant_tile;
+  k.d_index = l.d_index;
+  k.n_scales = l.n_scales;
+  k.rec_stride = l.rec_stride;
+  k.num_blocks = l.num_blocks;
+  k.rec_off = l.rec_off;
+  k.idx_key_off = l.idx_key_off;
+  k.idx_scale_off = l.idx_scale_off;
+  k.layer_stride = l.layer_stride;
+  k.block_stride = l.block_stride;
+  return k;
+}
+
+// Device error word (defined in api.cu); launchers receive its address.
+unsigned* device_error_word();
+int device_sm_count();
+
+smla_status_t launch_kvpack_store(const KernelLayout& L, void* pool, int layer, const void* latent,
+                                  const void* rope, const uint8_t* idx_k, const float* idx_scale,
+                                  const int64_t* slot_mapping, int n_tokens, cudaStream_t stream, unsigned* err);
+
+smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const void* pool, int layer,
+                                  const uint8_t* q_idx, const float* w, const int32_t* block_table, int bt_stride,
+                                  const int32_t* seq_lens, const int32_t* query_start_loc, int batch, int tok_begin,
+                                  int tok_end, int max_q, int max_ctx, float* scores, int64_t scores_stride,
+                                  cudaStream_t stream, unsigned* err);
+
+smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
+                          const int32_t* query_start_loc, int batch, int tok_begin, int tok_end, int32_t* topk_idx,
+                          cudaStream_t stream, unsigned* err);
+
+smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float softmax_scale, const void* pool,
+                            int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
+                            const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
+                            int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err);
+
+}  // namespace smla

@@ -1,0 +1,70 @@
+"""The C-ABI library builds, loads, and exports every symbol its header declares (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import paged_sparse_mla_gb300 as smla
+from paged_sparse_mla_gb300 import build_lib
+import oracle
+
+HEADER = os.path.join(build_lib.ROOT, "include", "smla.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build_lib.build()
+    return smla.lib()
+
+
+def _declared():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(\w+)\s*\(", text, flags=re.M)) - {"if"}
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert declared == set(smla.EXPORTED_SYMBOLS), declared ^ set(smla.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_layout_init_matches_oracle_layout(lib):
+    for args in [(64, 1, 512, 64, 128, 128, 1000), (16, 1, 64, 16, 64, 32, 32), (64, 3, 512, 64, 128, 128, 7)]:
+        lay = smla.layout_init(*args)
+        ref = oracle.PoolLayout(*args)
+        assert lay.rec_stride == ref.rec_stride and lay.rec_bytes == ref.rec_bytes
+        assert lay.idx_key_off == ref.idx_key_off and lay.idx_scale_off == ref.idx_scale_off
+        assert lay.layer_stride == ref.layer_stride and lay.block_stride == ref.block_stride
+        assert lay.pool_bytes == ref.pool_bytes
+
+
+@pytest.mark.parametrize("bad", [(0, 1, 512, 64, 128, 128, 10), (64, 1, 500, 64, 128, 128, 10),
+                                 (64, 1, 512, 64, 100, 128, 10), (64, 1, 512, 63, 128, 128, 10),
+                                 (64, 1, 512, 64, 128, 120, 10), (64, 0, 512, 64, 128, 128, 10)])
+def test_layout_init_rejects_bad_shapes(lib, bad):
+    with pytest.raises(smla.SmlaError) as e:
+        smla.layout_init(*bad)
+    assert e.value.code == 1
+
+
+def test_host_side_argument_checks(lib):
+    lay = smla.layout_init(64, 1, 512, 64, 128, 128, 10)
+    prm = smla.make_params(64, 64, 2048, 1 / 24)
+    L = ctypes.byref(lay)
+    P = ctypes.byref(prm)
+    # null descriptors / pointers are rejected before any device work
+    assert lib.kvpack_store(None, None, 0, None, None, None, None, None, 1, None) == 1
+    assert lib.kvpack_store(L, None, 0, None, None, None, None, None, 1, None) == 1
+    assert lib.kvpack_store(L, None, 0, None, None, None, None, None, 0, None) == 0   # nothing to do
+    assert lib.kvpack_store(L, ctypes.c_void_p(256), 5, None, None, None, None, None, 1, None) == 1  # bad layer
+    assert lib.smla_topk(P, None, 0, None, None, 1, 4, None, None) == 1
+    assert lib.smla_attend(L, P, None, 0, None, None, None, None, 0, None, 1, 3, None, None, None) == 1
+    assert lib.smla_decode(L, P, None, 0, None, None, None, None, None, None, None, None, None, None, 0, None,
+                           None, 1, 4, 1, 100, None, None, None, None, 0, None) == 1
+    assert lib.smla_workspace_size(L, P, 0, 100) == 0
+    assert lib.smla_workspace_size(L, P, 4, 1000) >= 4 * 1000 * 4 + 4 * 2048 * 4
+    assert lib.smla_status_string(4) == b"SMLA_ERR_BAD_INDEX"
+    assert lib.smla_version() >= 100
