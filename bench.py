@@ -1,0 +1,502 @@
+"""Benchmark of the paged top-k sparse-MLA hot path on GB300.
+
+One step = one call of the fused path (store of the step's new tokens ->
+indexer scores -> top-k -> latent attention) for one layer over one batch of
+the synthetic workload, inputs resident in HBM.  Default workload: the agentic
+MTP decode batch at ~128K context (64 sequences x 4 query tokens, lognormal
+contexts with median 142K, forked subagents sharing >= 96% of their blocks).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload 1..5] [--impl smla|reference]
+
+Prints one JSON line.  --impl reference times the CPU oracle (the plain numpy
+statement of the method) on a bounded sample of the same workload.  Under
+torchrun each rank runs an independent replica (the path has no exchange
+step), timing is the max over ranks, and value = all ranks' query tokens /
+that time.
+"""
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "sparse-MLA decode tokens/s and HBM GB/s (% of GB300 peak) at 128K context"
+UNIT = "tokens/s"
+L2_BYTES = 129 * 1024 * 1024
+KERNEL_SOURCES = {
+    "kvpack_store": "store.cu",
+    "smla_index_scores": "indexer.cu",
+    "smla_topk": "topk.cu",
+    "smla_attend": "attend.cu",
+}
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm=d["hbm_gbs"], bf16=d["bf16_tflops"], bf16_sus=d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                    src="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sus=1700.0, src="fallback")
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+                                         stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- accounting
+def accounting(wl, topk_host):
+    """Algorithmic bytes / flops per step for each kernel (see the design notes)."""
+    d = wl.dims
+    bs = d.block_size
+    seq_lens = wl.seq_lens.cpu().numpy().astype(np.int64)
+    qsl = wl.query_start_loc.cpu().numpy().astype(np.int64)
+    bt = wl.block_table.cpu().numpy().astype(np.int64)
+    T = wl.n_tokens
+    # positions of each query token
+    pos = np.empty(T, np.int64)
+    seq = np.empty(T, np.int64)
+    for b in range(wl.batch):
+        n_q = qsl[b + 1] - qsl[b]
+        pos[qsl[b]:qsl[b + 1]] = seq_lens[b] - n_q + np.arange(n_q)
+        seq[qsl[b]:qsl[b + 1]] = b
+    visible = int((pos + 1).sum())
+    # unique physical blocks read by the indexer (prefix-shared blocks once)
+    blocks = set()
+    logical_keys = 0
+    for b in range(wl.batch):
+        n = int(pos[qsl[b + 1] - 1] + 1)
+        nb = (n + bs - 1) // bs
+        blocks.update(bt[b, :nb].tolist())
+        logical_keys += n
+    uniq_keys = len(blocks) * bs
+    idx_rec = d.d_index + 4
+    rec = ((d.d_latent + 4 * (d.d_latent // d.quant_tile) + 2 * d.d_rope) + 15) // 16 * 16
+    q_idx_b = T * d.n_idx_heads * d.d_index + T * d.n_idx_heads * 4
+    acct = {}
+    acct["smla_index_scores"] = dict(
+        bytes=uniq_keys * idx_rec + q_idx_b + 4 * visible,
+        logical_bytes=logical_keys * idx_rec + q_idx_b + 4 * visible,
+        flops=2.0 * visible * d.n_idx_heads * d.d_index, flop_dtype="fp8")
+    acct["smla_topk"] = dict(bytes=4 * visible + 4 * T * d.top_k, flops=0.0, flop_dtype=None)
+    valid = topk_host >= 0
+    sel_slots = set()
+    for t in range(T):
+        j = topk_host[t][valid[t]].astype(np.int64)
+        sl = bt[seq[t], j // bs] * bs + j % bs
+        sel_slots.update(sl.tolist())
+    n_sel = int(valid.sum())
+    q_b = T * d.n_heads * (d.d_latent + d.d_rope) * 2
+    out_b = T * d.n_heads * d.d_latent * 2 + T * d.n_heads * 4
+    acct["smla_attend"] = dict(
+        bytes=len(sel_slots) * rec + q_b + out_b + 4 * T * d.top_k,
+        logical_bytes=n_sel * rec + q_b + out_b + 4 * T * d.top_k,
+        flops=2.0 * n_sel * d.n_heads * (2 * d.d_latent + d.d_rope), flop_dtype="bf16")
+    acct["kvpack_store"] = dict(bytes=T * (2 * d.d_latent + 2 * d.d_rope + d.d_index + 4 + 8) + T * (rec + idx_rec),
+                                flops=0.0, flop_dtype=None)
+    acct["_step"] = dict(bytes=sum(v["bytes"] for v in acct.values()),
+                         logical_bytes=sum(v.get("logical_bytes", v["bytes"]) for k, v in acct.items()),
+                         visible=visible, uniq_keys=uniq_keys, logical_keys=logical_keys, n_sel=n_sel,
+                         uniq_sel=len(sel_slots))
+    return acct
+
+
+def traffic_table():
+    """ncu DRAM bytes per launch recorded under profiles/, keyed by kernel source hash."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
+    if not os.path.exists(path):
+        return out
+    for line in open(path):
+        line = line.strip()
+        if not line or line.startswith("#"):
+            continue
+        parts = line.split()
+        if len(parts) >= 4:
+            out[(parts[0], parts[1])] = (parts[2], float(parts[3]))   # (kernel, workload) -> (sha, bytes)
+    return out
+
+
+def source_sha(kernel):
+    p = os.path.join(ROOT, "paged_sparse_mla_gb300", "csrc", KERNEL_SOURCES[kernel])
+    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch.distributed as dist
+    import paged_sparse_mla_gb300 as smla
+    from paged_sparse_mla_gb300 import build_lib
+    from paged_sparse_mla_gb300.workloads import make_config
+
+    rank, local_rank, world = dist_env()
+    torch.cuda.set_device(local_rank)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if rank == 0:
+        build_lib.build()
+    if world > 1:
+        dist.barrier()
+    smla.lib()
+    wl = make_config(args.workload, device="cuda")
+    d = wl.dims
+    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
+    pool = torch.zeros(lay.pool_bytes, dtype=torch.uint8, device="cuda")
+    s = wl.cached_slots
+    for c0 in range(0, s.numel(), 1 << 20):
+        sl = s[c0:c0 + (1 << 20)].contiguous()
+        smla.kvpack_store(lay, pool, 0, wl.slot_latent[sl].contiguous(), wl.slot_rope[sl].contiguous(),
+                          wl.slot_idx_k[sl].contiguous(), wl.slot_idx_s[sl].contiguous(), sl)
+    # the per-slot generator tensors are not needed any more
+    wl.slot_latent = wl.slot_rope = wl.slot_idx_k = wl.slot_idx_s = None
+    torch.cuda.empty_cache()
+    T = wl.n_tokens
+    ws = torch.empty(smla.workspace_size(lay, prm, T, wl.max_ctx), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
+    topk = torch.empty((T, d.top_k), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step(o=out, l=lse, q=wl.q, qpe=wl.q_pe, qi=wl.q_idx, w=wl.w, nl=wl.new_latent, nr=wl.new_rope,
+             nk=wl.new_idx_k, ns=wl.new_idx_s, sm=wl.slot_mapping, bt=wl.block_table, sq=wl.seq_lens,
+             qs=wl.query_start_loc):
+        smla.smla_decode(lay, prm, pool, 0, nl, nr, nk, ns, sm, q, qpe, qi, w, bt, sq, qs, wl.max_q, wl.max_ctx,
+                         o, l, ws, topk_idx_out=topk, stream=stream)
+
+    stride = (wl.max_ctx + 3) // 4 * 4
+    per_group = max(1, min(T, (256 << 20) // (stride * 4)))
+    n_groups = math.ceil(T / per_group)
+    launches_per_step = 1 + 3 * n_groups
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    err = smla.smla_get_last_error()
+    if err != 0:
+        raise RuntimeError(f"device error during warm-up: {smla.status_string(err)}")
+
+    # ---------------- timed region: K fused steps ----------------
+    clocks = ClockSampler(local_rank) if rank == 0 else None
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    clk = clocks.stop() if clocks else None
+    ms = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms = float(tt.item())
+    err = smla.smla_get_last_error()
+    if err != 0:
+        raise RuntimeError(f"device error in the timed region: {smla.status_string(err)}")
+    ms_step = ms / args.steps
+    value = world * T * args.steps / (ms / 1e3)
+
+    # ---------------- per-kernel timing: same kernels, separate calls, events on the launch stream ----------------
+    kern = {k: [] for k in ("kvpack_store", "smla_index_scores", "smla_topk", "smla_attend")}
+    # one launch of each kernel over all query tokens (the fused call splits long prefill into groups)
+    scores = torch.empty((T, stride), dtype=torch.float32, device="cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for it in range(args.warmup + args.steps):
+        ev[0].record(stream)
+        smla.kvpack_store(lay, pool, 0, wl.new_latent, wl.new_rope, wl.new_idx_k, wl.new_idx_s, wl.slot_mapping,
+                          stream=stream)
+        ev[1].record(stream)
+        smla.smla_index_scores(lay, prm, pool, 0, wl.q_idx, wl.w, wl.block_table, wl.seq_lens,
+                               wl.query_start_loc, wl.max_q, wl.max_ctx, scores, stream=stream)
+        ev[2].record(stream)
+        smla.smla_topk(prm, scores, wl.seq_lens, wl.query_start_loc, topk, stream=stream)
+        ev[3].record(stream)
+        smla.smla_attend(lay, prm, pool, 0, wl.q, wl.q_pe, topk, wl.block_table, wl.query_start_loc, out, lse,
+                         stream=stream)
+        ev[4].record(stream)
+        torch.cuda.synchronize()
+        if it >= args.warmup:
+            for k, (a, b) in zip(kern, [(0, 1), (1, 2), (2, 3), (3, 4)]):
+                kern[k].append(ev[a].elapsed_time(ev[b]))
+    kern_ms = {k: (sum(v) / len(v) if v else None) for k, v in kern.items()}
+    del scores
+    torch.cuda.empty_cache()
+
+    # ---------------- end to end: host buffers in, results out, every step ----------------
+    host_in = {n: getattr(wl, n).cpu().pin_memory() for n in
+               ("new_latent", "new_rope", "new_idx_k", "new_idx_s", "slot_mapping", "q", "q_pe", "q_idx", "w",
+                "block_table", "seq_lens", "query_start_loc")}
+    dev_in = {n: torch.empty_like(v, device="cuda") for n, v in host_in.items()}
+    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+
+    def e2e_step():
+        for n, v in host_in.items():
+            dev_in[n].copy_(v, non_blocking=True)
+        smla.smla_decode(lay, prm, pool, 0, dev_in["new_latent"], dev_in["new_rope"], dev_in["new_idx_k"],
+                         dev_in["new_idx_s"], dev_in["slot_mapping"], dev_in["q"], dev_in["q_pe"], dev_in["q_idx"],
+                         dev_in["w"], dev_in["block_table"], dev_in["seq_lens"], dev_in["query_start_loc"],
+                         wl.max_q, wl.max_ctx, out, lse, ws, topk_idx_out=topk, stream=stream)
+        host_out.copy_(out, non_blocking=True)
+        host_lse.copy_(lse, non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_e2e = e0.elapsed_time(e1)
+    if world > 1:
+        tt = torch.tensor([ms_e2e], device="cuda")
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_e2e = float(tt.item())
+    e2e_value = world * T * args.steps / (ms_e2e / 1e3)
+
+    if rank != 0:
+        dist.destroy_process_group()
+        return
+
+    # ---------------- roofline of the dominant kernel ----------------
+    acct = accounting(wl, topk.cpu().numpy())
+    pk = peaks()
+    tt = traffic_table()
+    dominant = max((k for k in kern_ms if kern_ms[k] is not None), key=lambda k: kern_ms[k], default=None)
+    roof = None
+    kernels = {}
+    for k, msk in kern_ms.items():
+        if msk is None:
+            continue
+        a = acct[k]
+        gbs = a["bytes"] / (msk / 1e3) / 1e9
+        fl = a["flops"] / (msk / 1e3) / 1e12 if a["flops"] else 0.0
+        kernels[k] = {"ms": round(msk, 4), "alg_bytes": a["bytes"], "alg_gbs": round(gbs, 1),
+                      "hbm_frac": round(gbs / pk["hbm"], 3)}
+        if a["flops"]:
+            fpk = pk["bf16"] * (2.0 if a["flop_dtype"] == "fp8" else 1.0)
+            kernels[k].update({"tflops": round(fl, 1), "tensor_frac": round(fl / fpk, 3),
+                               "tensor_peak": f"{fpk:.0f} ({'2x ' if a['flop_dtype'] == 'fp8' else ''}bf16 of {pk['src']})"})
+    if dominant is not None:
+        a = acct[dominant]
+        msk = kern_ms[dominant]
+        t_hbm = a["bytes"] / (pk["hbm"] * 1e9)
+        fpk = pk["bf16"] * (2.0 if a["flop_dtype"] == "fp8" else 1.0) if a["flops"] else None
+        t_ten = a["flops"] / (fpk * 1e12) if fpk else 0.0
+        wname = wl.name
+        tr = tt.get((dominant, wname))
+        traffic = tr[1] if tr is not None and tr[0] == source_sha(dominant) else None
+        if t_ten > t_hbm:
+            ach = a["flops"] / (msk / 1e3) / 1e12
+            roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fpk, 1),
+                    "unit": "TFLOP/s", "frac": round(ach / fpk, 4), "traffic": traffic,
+                    "peak_source": f"{'2 x ' if a['flop_dtype'] == 'fp8' else ''}bf16 burst of {pk['src']} (fp8:bf16 nominal 2:1)"}
+        else:
+            ach = a["bytes"] / (msk / 1e3) / 1e9
+            roof = {"kernel": dominant, "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"], "unit": "GB/s",
+                    "frac": round(ach / pk["hbm"], 4), "traffic": traffic, "peak_source": f"hbm copy of {pk['src']}"}
+        roof["alg_bytes_per_launch"] = a["bytes"]
+        roof["alg_flops_per_launch"] = a["flops"]
+
+    step_b = acct["_step"]["bytes"]
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3+bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": wl.batch, "query_tokens": T, "max_q_per_seq": wl.max_q,
+                   "mean_ctx": round(float(wl.seq_lens.float().mean()), 1), "max_ctx": wl.max_ctx,
+                   "top_k": d.top_k, "heads": d.n_heads, "idx_heads": d.n_idx_heads, "block_size": d.block_size,
+                   "pool_gb": round(lay.pool_bytes / 1e9, 3), "parallelism": f"replicas x{world}",
+                   "l2": f"inputs larger than L2: {step_b / 1e6:.0f} MB unique per step > 129 MB",
+                   "query_groups_per_step": n_groups},
+        "hbm_gbs": round(step_b / (ms_step / 1e3) / 1e9, 1),
+        "hbm_frac": round(step_b / (ms_step / 1e3) / 1e9 / pk["hbm"], 4),
+        "step_bytes": {"unique": step_b, "logical": acct["_step"]["logical_bytes"]},
+        "clocks": clk,
+        "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_step * args.steps,
+        "kernels": kernels,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- oracle (CPU) arm
+def oracle_sample(workload: int, budget_s: float, steps: int = 1):
+    """Time the CPU oracle on whole sequences of the workload until budget_s of work."""
+    import oracle
+    from paged_sparse_mla_gb300.workloads import make_config
+
+    def npy(t):
+        return t.detach().cpu().numpy()
+
+    def bits(t):
+        return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+    wl = make_config(workload, device="cpu")
+    d = wl.dims
+    lay = oracle.PoolLayout(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    rng = np.random.default_rng(7)
+    order = rng.permutation(wl.batch)
+    qsl = npy(wl.query_start_loc)
+    bt_all = npy(wl.block_table)
+    done_tokens, spent, seqs = 0, 0.0, []
+    for b in order:
+        n_cached = int(wl.seq_lens[b]) - int(qsl[b + 1] - qsl[b])
+        slots = oracle.context_slots(bt_all[b], n_cached, d.block_size)
+        pool = np.zeros(lay.pool_bytes, dtype=np.uint8)      # the cached context (not part of the timed step)
+        for c0 in range(0, slots.size, 1 << 17):
+            sc = torch.as_tensor(slots[c0:c0 + (1 << 17)])
+            oracle.kvpack_store(lay, pool, 0, bits(wl.slot_latent[sc]), bits(wl.slot_rope[sc]),
+                                npy(wl.slot_idx_k[sc]), npy(wl.slot_idx_s[sc]), sc.numpy())
+        rows = list(range(int(qsl[b]), int(qsl[b + 1])))
+        sm = npy(wl.slot_mapping).copy()
+        keep = np.zeros(sm.shape, bool)
+        keep[rows] = True
+        sm[~keep] = -1                           # store this sequence's new tokens only
+        t0 = time.perf_counter()
+        oracle.decode_step(lay, pool, 0, latent_new=bits(wl.new_latent), rope_new=bits(wl.new_rope),
+                           idxk_new=npy(wl.new_idx_k), idxs_new=npy(wl.new_idx_s), slot_mapping=sm, q=bits(wl.q),
+                           q_pe=bits(wl.q_pe), q_idx=npy(wl.q_idx), w=npy(wl.w), block_table=npy(wl.block_table),
+                           seq_lens=npy(wl.seq_lens), query_start_loc=qsl, top_k=wl.dims.top_k,
+                           sigma=wl.dims.softmax_scale, rows=rows)
+        spent += time.perf_counter() - t0
+        done_tokens += len(rows)
+        seqs.append(int(b))
+        if spent >= budget_s:
+            break
+    return wl, done_tokens, spent, seqs
+
+
+def cpu_baseline(workload: int, budget_s: float):
+    wl, n, spent, seqs = oracle_sample(workload, budget_s)
+    cores = len(os.sched_getaffinity(0))
+    return {"value": round(n / spent, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{len(seqs)} whole sequences ({n} query tokens) of {wl.name}, full store+indexer+top-k+attention "
+                      f"per query token in numpy float64 ({spent:.1f} s); numpy BLAS may use all {cores} cores"}
+
+
+def run_reference(args):
+    rank, _, world = dist_env()
+    if rank != 0:
+        return
+    tok, spent_total = 0, 0.0
+    per_step = max(2.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
+    seqs_all = []
+    for i in range(args.warmup + args.steps):
+        wl, n, spent, seqs = oracle_sample(args.workload, per_step)
+        if i >= args.warmup:
+            tok += n
+            spent_total += spent
+            seqs_all += seqs
+    value = tok / spent_total
+    cores = len(os.sched_getaffinity(0))
+    name = wl.name
+    line = {
+        "metric": METRIC, "value": round(value, 3), "unit": UNIT, "impl": "reference", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * spent_total / args.steps, 1),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": name, "sample_per_step_s": per_step},
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": f"per step: whole sequences of {name} until {per_step:.0f} s of oracle work"},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

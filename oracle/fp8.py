@@ -39,9 +39,13 @@ def e4m3_decode(codes) -> np.ndarray:
 
 
 def _floor_log2(a: np.ndarray) -> np.ndarray:
-    """floor(log2(a)) for a > 0, exactly (frexp gives a = f * 2^e, f in [0.5, 1))."""
-    _, e = np.frexp(a)
-    return e.astype(np.int64) - 1
+    """floor(log2(a)) for normal float64 a > 0: the unbiased exponent field of its IEEE bits."""
+    return ((a.view(np.uint64) >> np.uint64(52)) & np.uint64(0x7FF)).astype(np.int64) - 1023
+
+
+def _pow2(e: np.ndarray) -> np.ndarray:
+    """2.0 ** e for integer e in the normal float64 range, built from the exponent field."""
+    return ((e + 1023).astype(np.uint64) << np.uint64(52)).view(np.float64)
 
 
 def e4m3_encode(x) -> np.ndarray:
@@ -51,19 +55,28 @@ def e4m3_encode(x) -> np.ndarray:
     ties to the even mantissa: the spacing of E4M3 values is 2^-9 below 2^-6
     (subnormals) and 2^(floor(log2|x|) - 3) above.
     """
-    arr = np.asarray(x, dtype=np.float64)
+    shape = np.shape(x)
+    flat = np.asarray(x, dtype=np.float64).reshape(-1)
+    out = np.empty(flat.size, dtype=np.uint8)
+    for c0 in range(0, flat.size, 1 << 20):       # bounded temporaries
+        out[c0:c0 + (1 << 20)] = _encode_flat(flat[c0:c0 + (1 << 20)])
+    return out.reshape(shape)
+
+
+def _encode_flat(arr: np.ndarray) -> np.ndarray:
+    arr = np.ascontiguousarray(arr)
     nan = np.isnan(arr)
     sign = np.where(np.signbit(arr), 0x80, 0).astype(np.int64)
     a = np.minimum(np.abs(np.where(nan, 0.0, arr)), E4M3_MAX)   # satfinite clamp
     normal_in = a >= _MIN_NORMAL
     safe_a = np.where(normal_in, a, 1.0)
-    quantum = np.where(normal_in, np.ldexp(1.0, _floor_log2(safe_a) - 3), _SUB_QUANTUM)
+    quantum = np.where(normal_in, _pow2(_floor_log2(safe_a) - 3), _SUB_QUANTUM)
     v = np.rint(a / quantum) * quantum          # np.rint: round half to even; exact product
     v = np.minimum(v, E4M3_MAX)
     normal_out = v >= _MIN_NORMAL
     safe_v = np.where(normal_out, v, 1.0)
     e = _floor_log2(safe_v)
-    m = np.rint((safe_v / np.ldexp(1.0, e) - 1.0) * 8.0).astype(np.int64)
+    m = np.rint((safe_v / _pow2(e) - 1.0) * 8.0).astype(np.int64)
     code_normal = ((e + 7) << 3) | m
     code_sub = np.rint(v / _SUB_QUANTUM).astype(np.int64)
     code = np.where(normal_out, code_normal, code_sub) | sign
