@@ -196,7 +196,7 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     smla.lib()
-    wl = make_config(args.workload, device="cuda")
+    wl = make_config(args.workload, device="cuda", scale=args.scale)
     d = wl.dims
     lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
     prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
@@ -223,7 +223,7 @@ def run_gpu(args):
                          o, l, ws, topk_idx_out=topk, stream=stream)
 
     stride = (wl.max_ctx + 3) // 4 * 4
-    per_group = max(1, min(T, (256 << 20) // (stride * 4)))
+    per_group = max(1, min(T, (512 << 20) // (stride * 4)))
     n_groups = math.ceil(T / per_group)
     launches_per_step = 1 + 3 * n_groups
 
@@ -489,6 +489,8 @@ def main():
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--scale", type=float, default=1.0,
+                    help="shrink context lengths (profiler captures of a smaller case; not a bench line)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -10,7 +10,7 @@ namespace {
 __device__ unsigned g_error_word;
 
 constexpr int kMaxDevices = 64;
-constexpr size_t kScoreBudget = size_t(256) << 20;  // bytes of fp32 scores per query group
+constexpr size_t kScoreBudget = size_t(512) << 20;  // bytes of fp32 scores per query group
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 

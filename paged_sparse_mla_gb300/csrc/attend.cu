@@ -7,13 +7,13 @@
 // log-sum-exp statistics so partial results can be merged.
 //
 // Design (sm_103a, one persistent CTA per SM, one query token at a time):
-//   * 128 selected positions form a tile.  Producer warps (4-6) translate the
+//   * 128 selected positions form a tile.  Eleven producer warps translate the
 //     logical positions through the block table, read the 656-byte records
 //     (L2 prefetch of the next tile with cp.async.bulk.prefetch), dequantise the
 //     E4M3 latent with its per-128 fp32 scales to bf16, and write the tile as
 //     9 chunks of [128 keys x 64 dims] with the 128-byte swizzle (8 latent
 //     chunks + 1 rope chunk); the query is staged the same way (64 heads).
-//   * MMA1 (warp 7): S^T[key, head] = Khat[key, :] . q[head, :] over 576 dims,
+//   * MMA1 (warp 12): S^T[key, head] = Khat[key, :] . q[head, :] over 576 dims,
 //     M = 128 keys, N = 64 heads, fp32 in tensor memory.  TMEM lane = key.
 //   * Softmax (warps 0-3, thread = key): per-head tile maxima with a butterfly
 //     transpose-reduction across lanes, online softmax with lazy rescaling
@@ -32,9 +32,15 @@ namespace {
 
 constexpr int kTile = 128;     // keys per tile
 constexpr int kHeads = 64;     // MMA N: query heads (zero padded)
-constexpr int kProducerThreads = 96;               // warps 4-6
-constexpr int kMmaWarp = 7;
-constexpr int kThreads = 32 * 8;
+// Warp roles: warpgroup 0 = softmax (warps 0-3); warps 4-11 and 13-15 = producers;
+// warp 12 = MMA issuer.  setmaxnreg moves registers to the softmax warpgroup.
+constexpr int kProducerThreads = 32 * 11;
+constexpr int kMmaWarp = 12;
+constexpr int kThreads = 32 * 16;
+constexpr int kLaunchRegs = 128;       // per thread at launch (65536 / 512)
+constexpr int kSoftmaxRegs = 216;
+constexpr int kOtherRegs = 96;         // 128*216 + 384*96 = 64512 <= 512*128
+static_assert(128 * kSoftmaxRegs + 384 * kOtherRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -43,7 +49,7 @@ template <int NCH>
 struct __align__(1024) AttnSmem {
   uint8_t kv[NCH][kTile * 128];    // chunk c: [128 keys][64 dims] bf16, swizzled; chunk NCH-1: rope, then P^T
   uint8_t q[NCH][kHeads * 128];    // chunk c: [64 heads][64 dims] bf16, swizzled
-  const uint8_t* rec[kTile];       // record address per key of the tile being gathered (nullptr = masked)
+  const uint8_t* rec[2][kTile];    // record address per key, current and next tile (nullptr = masked)
   float red[4][kHeads];
   float m_tile[kHeads];
   float m_run[kHeads];
@@ -105,6 +111,56 @@ __device__ __forceinline__ uint4 load_bf16x8_padded(const uint16_t* src, int ava
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Loads for one batch of the producer unit stream (see the key-tile loop):
+// latent units fetch 16 E4M3 codes and their fp32 scale, rope units fetch 8
+// bf16 (zero padded past d_rope).  Masked keys (nullptr record) read as zero.
+constexpr int kBatch = 6;
+__device__ __forceinline__ void load_units(const uint8_t* const* rec, int u0, int n_lat, int n_units, int parts,
+                                           int DL, int DR, int qtile, int n_scales, bool rope16,
+                                           uint4 (&val)[kBatch], float (&sc)[kBatch]) {
+#pragma unroll
+  for (int b = 0; b < kBatch; ++b) {
+    const int u = u0 + b * kProducerThreads;
+    val[b] = make_uint4(0, 0, 0, 0);
+    sc[b] = 0.f;
+    if (u < n_lat) {
+      const uint8_t* r = rec[u / parts];
+      const int part = u % parts;
+      if (r != nullptr) {
+        val[b] = __ldg(reinterpret_cast<const uint4*>(r) + part);
+        sc[b] = __ldg(reinterpret_cast<const float*>(r + DL) + (part * 16) / qtile);
+      }
+    } else if (u < n_units) {
+      const int ur = u - n_lat, v = ur % 8;
+      const uint8_t* r = rec[ur / 8];
+      if (r != nullptr && v * 8 < DR) {
+        const uint8_t* src = r + DL + 4 * n_scales + v * 16;
+        if (rope16 && v * 8 + 8 <= DR)
+          val[b] = __ldg(reinterpret_cast<const uint4*>(src));
+        else
+          val[b] = load_bf16x8_padded(reinterpret_cast<const uint16_t*>(src), DR - v * 8);
+      }
+    }
+  }
+}
+
+// 16 E4M3 codes (little-endian in `codes`) times `sc` -> 16 bf16 in two 16-byte words.
+__device__ __forceinline__ void dequant16(const uint4& codes, float sc, uint4& o0, uint4& o1) {
+  const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t ow[8];
+#pragma unroll
+  for (int x = 0; x < 4; ++x) {
+    const __half2_raw h01 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] & 0xFFFFu), __NV_E4M3);
+    const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] >> 16), __NV_E4M3);
+    const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
+    const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
+    ow[2 * x] = pack_bf16x2(f01.x * sc, f01.y * sc);
+    ow[2 * x + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
+  }
+  o0 = make_uint4(ow[0], ow[1], ow[2], ow[3]);
+  o1 = make_uint4(ow[4], ow[5], ow[6], ow[7]);
+}
+
 // Number of 128-key tiles a row needs: one past the last valid entry.
 __device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
   int last = -1;
@@ -124,7 +180,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const KernelLayout& L = A.L;
-  const int DL = L.d_latent, DR = L.d_rope;
+  constexpr int DL = (NCH - 1) * 64;  // latent dims (8 chunks of 64 for 512)
+  const int DR = L.d_rope;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -151,11 +208,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
   const uint32_t tmem_s = tmem + 256;   // S^T: 64 columns
   volatile int* abort = &sm.abort;
 
-  if (warp >= 4 && warp < kMmaWarp) {
+  if (warp >= 4 && warp != kMmaWarp) {
     // ------------------------------ producers ------------------------------
-    const int ptid = threadIdx.x - 128;  // 0..95
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
+    const int ptid = threadIdx.x - 128 - (warp > kMmaWarp ? 32 : 0);  // 0..351
     uint32_t n = 0, nw = 0, kk = 0;
-    const int parts = DL / 16;           // 16-code parts per record
+    constexpr int parts = DL / 16;       // 16-code parts per record
     const bool rope16 = ((DL + 4 * L.n_scales) % 16) == 0;
     for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
       const int t = A.tok_begin + tr;
@@ -188,13 +246,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       fence_proxy_async();
       mbar_arrive(&sm.q_full);
       // ---- key tiles ----
-      bool ok = true;
-      for (int tile = 0; tile < ntiles; ++tile, ++kk) {
-        if (!mbar_wait(&sm.kv_empty, (kk & 1) ^ 1, A.err, abort)) {
-          ok = false;
-          break;
-        }
-        named_bar_sync(2, kProducerThreads);  // previous tile's rec[] fully consumed
+      // Unit stream of one tile: units [0, 128*parts) are 16-code latent pieces
+      // (key r = u / parts), units [128*parts, 128*(parts+8)) are 16-byte rope pieces.
+      constexpr int n_lat = kTile * parts;
+      constexpr int n_units = n_lat + kTile * 8;
+      auto fill_rec = [&](int tile, int buf) {
         for (int rr = ptid; rr < kTile; rr += kProducerThreads) {
           const int e = tile * kTile + rr;
           const int j = e < A.top_k ? __ldg(idx + e) : -1;
@@ -206,76 +262,65 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
             } else {
               r = A.pool + static_cast<int64_t>(blk) * L.block_stride + static_cast<int64_t>(A.layer) * L.layer_stride +
                   L.rec_off + static_cast<int64_t>(j % L.block_size) * L.rec_stride;
+              prefetch_l2_bulk(r, static_cast<uint32_t>(L.rec_stride));
             }
           }
-          sm.rec[rr] = r;
-          // warm L2 with the next tile's record
-          const int e2 = e + kTile;
-          if (e2 < A.top_k) {
-            const int j2 = __ldg(idx + e2);
-            if (j2 >= 0) {
-              const int blk2 = __ldg(bt + j2 / L.block_size);
-              if (blk2 >= 0 && blk2 < L.num_blocks)
-                prefetch_l2_bulk(A.pool + static_cast<int64_t>(blk2) * L.block_stride +
-                                     static_cast<int64_t>(A.layer) * L.layer_stride + L.rec_off +
-                                     static_cast<int64_t>(j2 % L.block_size) * L.rec_stride,
-                                 static_cast<uint32_t>(L.rec_stride));
-            }
-          }
+          sm.rec[buf][rr] = r;
         }
-        named_bar_sync(2, kProducerThreads);
-        // latent: 16 E4M3 codes -> 16 bf16 (two 16-byte units) per step
-        for (int u = ptid; u < kTile * parts; u += kProducerThreads) {
-          const int r = u / parts, part = u % parts;
-          const uint8_t* rec = sm.rec[r];
-          uint4 o0 = make_uint4(0, 0, 0, 0), o1 = make_uint4(0, 0, 0, 0);
-          if (rec != nullptr) {
-            const uint4 codes = __ldg(reinterpret_cast<const uint4*>(rec) + part);
-            const float sc = __ldg(reinterpret_cast<const float*>(rec + DL) + (part * 16) / L.quant_tile);
-            const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
-            uint32_t ow[8];
+      };
+      fill_rec(0, 0);
+      named_bar_sync(2, kProducerThreads);
+      bool ok = true;
+      for (int tile = 0; tile < ntiles; ++tile, ++kk) {
+        const uint8_t* const* rec = sm.rec[tile & 1];
+        // first batch of loads is issued before waiting for the tile buffer
+        uint4 cur[kBatch];
+        float csc[kBatch];
+        load_units(rec, ptid, n_lat, n_units, parts, DL, DR, L.quant_tile, L.n_scales, rope16, cur, csc);
+        if (tile + 1 < ntiles) fill_rec(tile + 1, (tile + 1) & 1);  // addresses (and L2 warm-up) one tile ahead
+        if (!mbar_wait(&sm.kv_empty, (kk & 1) ^ 1, A.err, abort)) {
+          ok = false;
+          break;
+        }
+        for (int base = 0; base < n_units; base += kBatch * kProducerThreads) {
+          uint4 nxt[kBatch];
+          float nsc[kBatch];
+          const int nbase = base + kBatch * kProducerThreads;
+          if (nbase < n_units)
+            load_units(rec, nbase + ptid, n_lat, n_units, parts, DL, DR, L.quant_tile, L.n_scales, rope16, nxt, nsc);
 #pragma unroll
-            for (int x = 0; x < 4; ++x) {
-              const __half2_raw h01 =
-                  __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] & 0xFFFFu), __NV_E4M3);
-              const __half2_raw h23 =
-                  __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] >> 16), __NV_E4M3);
-              const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
-              const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-              ow[2 * x] = pack_bf16x2(f01.x * sc, f01.y * sc);
-              ow[2 * x + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
-            }
-            o0 = make_uint4(ow[0], ow[1], ow[2], ow[3]);
-            o1 = make_uint4(ow[4], ow[5], ow[6], ow[7]);
-          }
-          const int d0 = part * 16;
-          const int c = d0 / 64, v0 = (d0 % 64) / 8;
-          *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0)]) = o0;
-          *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0 + 1)]) = o1;
-        }
-        // rope (bf16) copied into the last chunk, zero padded to 64 dims
-        for (int u = ptid; u < kTile * 8; u += kProducerThreads) {
-          const int r = u / 8, v = u % 8;
-          const uint8_t* rec = sm.rec[r];
-          uint4 val = make_uint4(0, 0, 0, 0);
-          if (rec != nullptr && v * 8 < DR) {
-            const uint8_t* src = rec + DL + 4 * L.n_scales + v * 16;
-            if (rope16 && v * 8 + 8 <= DR) {
-              val = __ldg(reinterpret_cast<const uint4*>(src));
+          for (int b = 0; b < kBatch; ++b) {
+            const int u = base + ptid + b * kProducerThreads;
+            if (u >= n_units) break;
+            if (u < n_lat) {
+              const int r = u / parts, part = u % parts;
+              uint4 o0, o1;
+              dequant16(cur[b], csc[b], o0, o1);
+              const int d0 = part * 16;
+              const int c = d0 / 64, v0 = (d0 % 64) / 8;
+              *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0)]) = o0;
+              *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0 + 1)]) = o1;
             } else {
-              val = load_bf16x8_padded(reinterpret_cast<const uint16_t*>(src), DR - v * 8);
+              const int ur = u - n_lat, r = ur / 8, v = ur % 8;
+              *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(r, v)]) = cur[b];
             }
           }
-          *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(r, v)]) = val;
+#pragma unroll
+          for (int b = 0; b < kBatch; ++b) {
+            cur[b] = nxt[b];
+            csc[b] = nsc[b];
+          }
         }
         fence_proxy_async();
         mbar_arrive(&sm.kv_full);
+        named_bar_sync(2, kProducerThreads);  // next tile's addresses complete; this tile's reads done
       }
       if (!ok) break;
       ++nw;
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (lane == 0) {
       uint32_t n = 0, nw = 0, kk = 0;
       bool issued = false;
@@ -331,6 +376,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
     }
   } else {
     // ------------------------------ softmax + epilogue (warps 0-3) ------------------------------
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
     const int tid = threadIdx.x;  // key row of the tile / dim row of an O^T tile
     const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
     uint32_t n = 0, nw = 0, kk = 0;
@@ -402,7 +448,9 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
 #pragma unroll
             for (int h = 0; h < kHeads; ++h) l_part[h] *= sm.alpha[h];
             const int dtiles = (DL + 127) / 128;
+#pragma unroll 1
             for (int d2 = 0; d2 < dtiles; ++d2) {
+#pragma unroll 1
               for (int hh = 0; hh < kHeads; hh += 32) {
                 uint32_t o[32];
                 tmem_ld32(tmem_o + lane_base + d2 * kHeads + hh, o);
@@ -461,8 +509,10 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       }
       named_bar_sync(1, 128);
       const int dtiles = (DL + 127) / 128;
+#pragma unroll 1
       for (int d2 = 0; d2 < dtiles; ++d2) {
         const int d = d2 * 128 + tid;
+#pragma unroll 1
         for (int hh = 0; hh < kHeads; hh += 32) {
           uint32_t o[32];
           tmem_ld32(tmem_o + lane_base + d2 * kHeads + hh, o);
@@ -500,6 +550,11 @@ smla_status_t launch_nch(const AttnArgs& A, cudaStream_t stream) {
     if (cudaFuncSetAttribute(attend_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
+    // setmaxnreg.inc can only draw on the registers the CTA was launched with;
+    // refuse to launch if the compiled allocation does not cover the split.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH>) != cudaSuccess) return SMLA_ERR_CUDA;
+    if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set = true;
   }
   const int grid = min(A.n_rows, device_sm_count());

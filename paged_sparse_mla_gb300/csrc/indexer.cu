@@ -13,13 +13,14 @@
 //   * the contraction is one FP8 tcgen05.mma per 32 key dims with the 128 keys
 //     of a tile as M (TMEM lane = key) and the group's query heads as N
 //     (<= 4 tokens x 64 heads = 256), accumulated in fp32 in tensor memory;
-//   * warps 0-3 (epilogue) read a key's row of head dot products from TMEM and
-//     reduce sum_h w * ReLU(.) per token in registers -- no cross-thread
-//     reduction -- then scale by s_I[j] and store the fp32 score (coalesced);
-//   * warps 4-7 (producers) stream 128-key tiles of the indexer-key region of
+//   * warps 0-7 (epilogue; warps w and w+4 share TMEM lanes 32*(w%4).. and
+//     split the group's tokens) read a key's row of head dot products from
+//     TMEM and reduce sum_h w * ReLU(.) per token in registers -- no
+//     cross-thread reduction -- then scale by s_I[j] and store the fp32 score;
+//   * warps 8-11 (producers) stream 128-key tiles of the indexer-key region of
 //     each block through the block table with 16-byte cp.async into 128-byte
 //     swizzled stages (one warp per tile, four tiles in flight per CTA);
-//   * warp 8 issues the MMAs and owns the tensor-memory allocation.
+//   * warp 12 issues the MMAs and owns the tensor-memory allocation.
 #include "smla_internal.h"
 
 namespace smla {
@@ -29,14 +30,17 @@ constexpr int kTile = 128;         // keys per tile (MMA M)
 constexpr int kGroup = 4;          // query tokens per item (MMA N = kGroup * n_idx_heads)
 constexpr int kStages = 8;         // key-tile ring
 constexpr int kChunkTiles = 16;    // tiles per work item (2048 keys)
+constexpr int kEpiWarps = 8;       // two warps per TMEM sub-partition, splitting the group's tokens
 constexpr int kProducers = 4;      // producer warps
-constexpr int kThreads = 32 * (4 + kProducers + 1);
+constexpr int kMmaWarp = kEpiWarps + kProducers;
+constexpr int kThreads = 32 * (kEpiWarps + kProducers + 1);
 constexpr int kMaxN = 256;         // MMA N limit
 
 struct __align__(1024) IdxSmem {
   uint8_t keys[kStages][kTile * 128];   // 16 KB per stage, 1024-aligned
   uint8_t q[2][kMaxN * 128];            // 32 KB per buffer
-  float w[kGroup * 64];                 // epilogue-owned weights of the current item
+  float kscale[kStages][kTile];         // s_I of the tile's keys, loaded with the keys
+  float4 w[kGroup * 64 / 4];            // epilogue-owned weights of the current item
   uint64_t key_full[kStages], key_empty[kStages];
   uint64_t q_full[2], q_empty[2];
   uint64_t acc_full[2], acc_empty[2];
@@ -106,42 +110,51 @@ __device__ __forceinline__ int mma_n(int n_grp, int heads) {
   return max(16, (n + 15) & ~15);
 }
 
+template <int kH, int kD, int kBS>
 __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs A) {
   extern __shared__ uint8_t smem_raw[];
   IdxSmem& sm = *reinterpret_cast<IdxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const int n_items = A.n_chunks * A.batch * A.n_groups;
-  const int H = A.n_idx_heads;
-  const int D = A.L.d_index;
+  constexpr int H = kH;
+  constexpr int D = kD;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(&sm.key_full[s], 32);
-      mbar_init(&sm.key_empty[s], 1);
+      mbar_init(&sm.key_empty[s], 1 + kEpiWarps);  // MMA done + every epilogue warp read the scales
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.q_full[i], 32);
       mbar_init(&sm.q_empty[i], 1);
       mbar_init(&sm.acc_full[i], 1);
-      mbar_init(&sm.acc_empty[i], 128);
+      mbar_init(&sm.acc_empty[i], 32 * kEpiWarps);
     }
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
     mbar_fence_init();
   }
-  if (warp == 8) tmem_alloc(&sm.tmem_slot, 512);
+  if (warp == kMmaWarp) tmem_alloc(&sm.tmem_slot, 512);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
   volatile int* abort = &sm.abort;
 
-  if (warp >= 4 && warp < 4 + kProducers) {
+  if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ------------------------------ producers ------------------------------
-    const int pw = warp - 4;
+    // Lane l always copies 16-byte chunk (l % kCh) of rows l / kCh + i * kRowStep;
+    // a tile spans kTile / kBS blocks whose bases lanes 0.. load once per tile.
+    constexpr int kCh = kD / 16;
+    constexpr int kRowStep = 32 / kCh;
+    constexpr int kIters = kTile / kRowStep;
+    constexpr int kBlocks = kTile / kBS;
+    static_assert(kTile % kBS == 0 && kBS % kRowStep == 0 && kBlocks <= 32 && kBS % 4 == 0, "tile geometry");
+    const int pw = warp - kEpiWarps;
+    const int ch = lane % kCh, r0 = lane / kCh;
+    const int64_t layer_off = static_cast<int64_t>(A.layer) * A.L.layer_stride;
     uint32_t k = 0, nitem = 0;
-    const int chunks_per_row = D / 16;
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const Item it = decode_item(A, item);
       if (!it.valid) continue;
@@ -151,11 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         if (!mbar_wait(&sm.q_empty[qb], ((nitem >> 1) & 1) ^ 1, A.err, abort)) break;
         const int rows = it.n_grp * H;
         const uint32_t qbase = smem_u32(sm.q[qb]);
-        for (int u = lane; u < rows * chunks_per_row; u += 32) {
-          const int r = u / chunks_per_row, ch = u % chunks_per_row;
-          const uint8_t* src = A.q_idx + (static_cast<int64_t>(it.t0) * H + r) * D + ch * 16;
-          cp_async16(qbase + sw128_off(r, ch), src, 16);
-        }
+        const uint8_t* qsrc = A.q_idx + static_cast<int64_t>(it.t0) * H * kD + ch * 16;
+        for (int r = r0; r < rows; r += kRowStep) cp_async16(qbase + sw128_off(r, ch), qsrc + r * kD, 16);
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async();
@@ -164,26 +174,34 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       for (int tile = 0; tile < it.n_tiles; ++tile, ++k) {
         if (static_cast<int>(k % kProducers) != pw) continue;
         const int s = k % kStages;
+        const int j0 = it.key_begin + tile * kTile;
+        unsigned long long kbase = 0;  // lane b < kBlocks: base of block b of the tile (0 = skip)
+        if (lane < kBlocks && j0 + lane * kBS < it.key_end) {
+          const int blk = __ldg(bt + (j0 + lane * kBS) / kBS);
+          if (blk < 0 || blk >= A.L.num_blocks) {
+            latch_error(A.err, SMLA_ERR_BAD_INDEX);
+          } else {
+            kbase = reinterpret_cast<unsigned long long>(A.pool + static_cast<int64_t>(blk) * A.L.block_stride + layer_off);
+          }
+        }
         if (!mbar_wait(&sm.key_empty[s], ((k / kStages) & 1) ^ 1, A.err, abort)) break;
         const uint32_t base = smem_u32(sm.keys[s]);
-        const int j0 = it.key_begin + tile * kTile;
-        for (int u = lane; u < kTile * chunks_per_row; u += 32) {
-          const int r = u / chunks_per_row, ch = u % chunks_per_row;
-          const int j = j0 + r;
-          const uint8_t* src = A.pool;
-          uint32_t bytes = 0;
-          if (j < it.key_end) {
-            int blk = __ldg(bt + j / A.L.block_size);
-            if (blk < 0 || blk >= A.L.num_blocks) {
-              latch_error(A.err, SMLA_ERR_BAD_INDEX);
-            } else {
-              src = A.pool + static_cast<int64_t>(blk) * A.L.block_stride +
-                    static_cast<int64_t>(A.layer) * A.L.layer_stride + A.L.idx_key_off +
-                    static_cast<int64_t>(j % A.L.block_size) * D + ch * 16;
-              bytes = 16;
-            }
-          }
-          cp_async16(base + sw128_off(r, ch), src, bytes);
+#pragma unroll
+        for (int i = 0; i < kIters; ++i) {
+          const int r = r0 + i * kRowStep;
+          const unsigned long long b = __shfl_sync(0xffffffffu, kbase, (i * kRowStep) / kBS);
+          const bool ok = b != 0 && j0 + r < it.key_end;
+          const uint8_t* src = ok ? reinterpret_cast<const uint8_t*>(b) + A.L.idx_key_off + (r % kBS) * kD + ch * 16
+                                  : A.pool;
+          cp_async16(base + sw128_off(r, ch), src, ok ? 16u : 0u);
+        }
+        {
+          // key scales: lane l copies keys 4l..4l+3 (never straddling a block)
+          const unsigned long long b = __shfl_sync(0xffffffffu, kbase, (4 * lane) / kBS);
+          const bool ok = b != 0 && j0 + 4 * lane < it.key_end;
+          const uint8_t* src =
+              ok ? reinterpret_cast<const uint8_t*>(b) + A.L.idx_scale_off + ((4 * lane) % kBS) * 4 : A.pool;
+          cp_async16(smem_u32(&sm.kscale[s][4 * lane]), src, ok ? 16u : 0u);
         }
         cp_async_commit();
         cp_async_wait<0>();
@@ -192,7 +210,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       }
       ++nitem;
     }
-  } else if (warp == 8) {
+  } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
     if (lane == 0) {
       uint32_t k = 0, nitem = 0, a = 0;
@@ -234,50 +252,51 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       }
     }
   } else {
-    // ------------------------------ epilogue (warps 0-3) ------------------------------
-    const int row = threadIdx.x;  // TMEM lane == key within the tile
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ------------------------------ epilogue (warps 0-7) ------------------------------
+    const int row = (warp & 3) * 32 + lane;  // TMEM lane == key within the tile
+    const int half = warp >> 2;              // tokens half, half+2 of the group
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t a = 0;
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const Item it = decode_item(A, item);
       if (!it.valid) continue;
-      named_bar_sync(1, 128);
-      for (int i = row; i < it.n_grp * H; i += 128) sm.w[i] = __ldg(A.w + static_cast<int64_t>(it.t0) * H + i);
-      named_bar_sync(1, 128);
-      const int32_t* bt = A.block_table + static_cast<int64_t>(it.b) * A.bt_stride;
+      named_bar_sync(1, 32 * kEpiWarps);
+      float* wf = reinterpret_cast<float*>(sm.w);
+      for (int i = threadIdx.x; i < it.n_grp * H; i += 32 * kEpiWarps)
+        wf[i] = __ldg(A.w + static_cast<int64_t>(it.t0) * H + i);
+      named_bar_sync(1, 32 * kEpiWarps);
       bool ok = true;
       for (int tile = 0; tile < it.n_tiles; ++tile, ++a) {
         const int j = it.key_begin + tile * kTile + row;
-        float s_key = 0.f;
-        if (j < it.key_end) {
-          const int blk = __ldg(bt + j / A.L.block_size);
-          if (blk >= 0 && blk < A.L.num_blocks) {
-            s_key = __ldg(reinterpret_cast<const float*>(A.pool + static_cast<int64_t>(blk) * A.L.block_stride +
-                                                         static_cast<int64_t>(A.layer) * A.L.layer_stride +
-                                                         A.L.idx_scale_off) +
-                          (j % A.L.block_size));
-          }
-        }
         const int ab = a & 1;
         if (!mbar_wait(&sm.acc_full[ab], (a >> 1) & 1, A.err, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        for (int i = 0; i < it.n_grp; ++i) {
-          float acc = 0.f;
+        const int st = a % kStages;  // the MMA consumed global tile a from stage a % kStages
+        const float s_key = sm.kscale[st][row];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.key_empty[st]);
+        for (int i = half; i < it.n_grp; i += 2) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
           for (int h0 = 0; h0 < H; h0 += 32) {
             uint32_t v[32];
             tmem_ld32(tmem + lane_base + ab * 256 + i * H + h0, v);
             tmem_ld_wait();
-            const int hn = min(32, H - h0);
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              if (x < hn) acc = fmaf(fmaxf(__uint_as_float(v[x]), 0.f), sm.w[i * H + h0 + x], acc);
+            for (int x = 0; x < 32 && h0 + x < H; x += 4) {
+              const float4 wv = sm.w[(i * H + h0 + x) / 4];
+              acc[0] = fmaf(fmaxf(__uint_as_float(v[x]), 0.f), wv.x, acc[0]);
+              acc[1] = fmaf(fmaxf(__uint_as_float(v[x + 1]), 0.f), wv.y, acc[1]);
+              acc[2] = fmaf(fmaxf(__uint_as_float(v[x + 2]), 0.f), wv.z, acc[2]);
+              acc[3] = fmaf(fmaxf(__uint_as_float(v[x + 3]), 0.f), wv.w, acc[3]);
             }
           }
+          const float total = (acc[0] + acc[1]) + (acc[2] + acc[3]);
           if (j <= it.p_first + i && j < it.key_end) {
-            A.scores[static_cast<int64_t>(it.t0 + i - A.tok_begin) * A.scores_stride + j] = acc * s_key;
+            A.scores[static_cast<int64_t>(it.t0 + i - A.tok_begin) * A.scores_stride + j] = total * s_key;
           }
         }
         tc_fence_before();
@@ -289,10 +308,24 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
 
   tc_fence_before();
   __syncthreads();
-  if (warp == 8) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+template <int kH, int kD, int kBS>
+smla_status_t launch_shape(const IdxArgs& A, int grid, cudaStream_t stream) {
+  const size_t smem = sizeof(IdxSmem) + 1024;
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(index_scores_kernel<kH, kD, kBS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    attr_set = true;
+  }
+  index_scores_kernel<kH, kD, kBS><<<grid, kThreads, smem, stream>>>(A);
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
 }  // namespace
@@ -327,18 +360,13 @@ smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const 
   A.err = err;
   const long long items = static_cast<long long>(A.n_chunks) * batch * A.n_groups;
   if (items <= 0) return SMLA_OK;
-  const size_t smem = sizeof(IdxSmem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(index_scores_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return SMLA_ERR_CUDA;
-    attr_set = true;
-  }
   const long long sms = device_sm_count();
   const int grid = static_cast<int>(items < sms ? items : sms);
-  index_scores_kernel<<<grid, kThreads, smem, stream>>>(A);
-  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  // Shapes built into the library: (indexer heads, key dims, block size).
+  if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 64) return launch_shape<64, 128, 64>(A, grid, stream);
+  if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 16) return launch_shape<64, 128, 16>(A, grid, stream);
+  if (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16) return launch_shape<4, 32, 16>(A, grid, stream);
+  return SMLA_ERR_UNSUPPORTED;
 }
 
 }  // namespace smla

@@ -4,14 +4,17 @@
 // [AgentX "DeepSeek V4"]: one global top-k per token; [AgentX "Closing the
 // loop: kernels"] names a dedicated top-k path among the kernels that matter.
 //
-// One CTA per query row.  Scores map to order-preserving 32-bit keys
-// (-0 folded onto +0).  A radix select over the key bits (12, 12, then 8 bits,
-// each pass a shared-memory histogram of the elements that still match the
-// bits fixed so far, with warp-aggregated increments) finds the k-th largest
-// key T and how many elements equal to T are still needed.  The selection pass
-// then gives each thread a contiguous segment of the row: counts of "> T" and
-// "== T" per segment, two block scans (tie rank, output slot), and a second
-// read of the segment writes the kept positions in ascending order.
+// One CTA per query row; scores map to order-preserving 32-bit keys (-0 folded
+// onto +0).  Fast path, two coalesced reads of the row:
+//   1. a 4096-bin histogram of the top 12 key bits (warp-aggregated shared
+//      memory increments) gives the bin B holding the k-th largest key;
+//   2. elements in bins above B are kept outright; elements of bin B are
+//      collected as 64-bit (key, ~position) pairs in shared memory.
+// A bitonic sort of the candidates (key descending, position ascending)
+// supplies the remaining winners, and a bitonic sort of the k kept positions
+// writes them in ascending order.  If bin B holds more candidates than shared
+// memory does, the row falls back to a radix select over all 32 key bits
+// (three histogram passes) and an index-ordered selection pass.
 #include "smla_internal.h"
 
 namespace smla {
@@ -20,6 +23,16 @@ namespace {
 constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;
+constexpr int kCap = 8192;     // candidate capacity of the fast path (power of two)
+constexpr int kMaxK = 4096;    // largest k of the fast path (power of two)
+
+struct TopkSmem {
+  int hist[kBins];
+  unsigned long long cand[kCap];
+  int sel[kMaxK];
+  int warp_tot[32];
+  int n_sel, n_cand, sel_bin, sel_above;
+};
 
 __device__ __forceinline__ uint32_t order_key(float x) {
   uint32_t u = __float_as_uint(x + 0.0f);  // -0 -> +0
@@ -52,27 +65,107 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_tot, int& t
   return x - v + (warp > 0 ? warp_tot[warp - 1] : 0);
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __restrict__ scores, int64_t stride,
-                                                        const int32_t* __restrict__ seq_lens,
-                                                        const int32_t* __restrict__ qsl, int batch, int tok_begin,
-                                                        int32_t* __restrict__ out) {
-  __shared__ int hist[kBins];
-  __shared__ int warp_tot[32];
-  __shared__ int sel_bin, sel_above;
-  const int row = blockIdx.x;
-  const int t = tok_begin + row;
-  const int b = seq_of_token(qsl, batch, t);
-  const int q0 = __ldg(qsl + b), n_q = __ldg(qsl + b + 1) - q0;
-  const int n = __ldg(seq_lens + b) - n_q + (t - q0) + 1;  // positions 0..p
-  const float* s = scores + static_cast<int64_t>(row) * stride;
-  int32_t* o = out + static_cast<int64_t>(row) * k;
-
-  if (n <= k) {
-    for (int i = threadIdx.x; i < k; i += kThreads) o[i] = i < n ? i : -1;
-    return;
+// Histogram of ((key >> shift) & bmask) over elements with (key & mask) == prefix.
+__device__ __forceinline__ void add_to_hist(int* hist, uint32_t key, bool in_row, uint32_t mask, uint32_t prefix,
+                                            int shift, uint32_t bmask) {
+  const bool hit = in_row && (key & mask) == prefix;
+  const uint32_t bin = (key >> shift) & bmask;
+  const uint32_t active = __ballot_sync(0xffffffffu, hit);
+  if (hit) {
+    const uint32_t peers = __match_any_sync(active, bin);
+    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
   }
+}
 
-  // ---- radix select of the k-th largest key ----
+// Visit every element of the row (float4 loads when the row is 16-byte aligned).
+template <typename F>
+__device__ __forceinline__ void for_row(const float* s, int n, F&& f) {
+  if ((reinterpret_cast<uintptr_t>(s) & 15) == 0) {
+    const int n4 = n & ~3;
+    for (int base = threadIdx.x * 4; base < ((n + 4 * kThreads - 1) / (4 * kThreads)) * 4 * kThreads;
+         base += 4 * kThreads) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (base < n4) {
+        v = __ldg(reinterpret_cast<const float4*>(s + base));
+      } else if (base < n) {
+        v.x = __ldg(s + base);
+        if (base + 1 < n) v.y = __ldg(s + base + 1);
+        if (base + 2 < n) v.z = __ldg(s + base + 2);
+      }
+      f(base, v.x, base < n);
+      f(base + 1, v.y, base + 1 < n);
+      f(base + 2, v.z, base + 2 < n);
+      f(base + 3, v.w, base + 3 < n);
+    }
+  } else {
+    for (int base = 0; base < n; base += kThreads) {
+      const int j = base + threadIdx.x;
+      f(j, j < n ? __ldg(s + j) : 0.f, j < n);
+    }
+  }
+}
+
+// Pick the bin B (scanning from the top) with count(> B) < remaining <= count(>= B).
+__device__ __forceinline__ void find_bin(TopkSmem& sm, int nb, int remaining) {
+  const int per = nb / kThreads > 0 ? nb / kThreads : 1;
+  const bool owns = threadIdx.x * per < nb;
+  const int hi_bin = nb - 1 - threadIdx.x * per;
+  int local = 0;
+  if (owns)
+    for (int x = 0; x < per; ++x) local += sm.hist[hi_bin - x];
+  int total;
+  const int before = block_exclusive_scan(owns ? local : 0, sm.warp_tot, total);
+  if (owns && before < remaining && before + local >= remaining) {
+    int acc = before;
+    for (int x = 0; x < per; ++x) {
+      const int c = sm.hist[hi_bin - x];
+      if (acc + c >= remaining) {
+        sm.sel_bin = hi_bin - x;
+        sm.sel_above = acc;
+        break;
+      }
+      acc += c;
+    }
+  }
+  __syncthreads();
+}
+
+template <typename T, bool kDescending>
+__device__ __forceinline__ void bitonic_sort(T* a, int m) {
+  for (int size = 2; size <= m; size <<= 1) {
+    for (int stride = size >> 1; stride > 0; stride >>= 1) {
+      for (int i = threadIdx.x; i < m / 2; i += kThreads) {
+        const int lo = 2 * i - (i & (stride - 1));
+        const int hi = lo + stride;
+        const bool up = ((lo & size) == 0) != kDescending;
+        const T x = a[lo], y = a[hi];
+        if ((x > y) == up) {
+          a[lo] = y;
+          a[hi] = x;
+        }
+      }
+      __syncthreads();
+    }
+  }
+}
+
+// Warp-aggregated append of `v` to list[counter++] for the lanes with `pred`.
+template <typename T>
+__device__ __forceinline__ void warp_append(bool pred, T v, T* list, int* counter, int cap) {
+  const uint32_t m = __ballot_sync(0xffffffffu, pred);
+  if (m == 0) return;
+  const int lane = threadIdx.x & 31;
+  const int leader = __ffs(m) - 1;
+  int base = 0;
+  if (lane == leader) base = atomicAdd(counter, __popc(m));
+  base = __shfl_sync(0xffffffffu, base, leader);
+  if (pred) {
+    const int pos = base + __popc(m & ((1u << lane) - 1u));
+    if (pos < cap) list[pos] = v;
+  }
+}
+
+__device__ void topk_slow(TopkSmem& sm, const float* s, int n, int k, int32_t* o) {
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
   const int shifts[3] = {20, 8, 0};
@@ -81,57 +174,21 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     const int shift = shifts[pass];
     const uint32_t bmask = (1u << widths[pass]) - 1u;
     const int nb = 1 << widths[pass];
-    for (int i = threadIdx.x; i < nb; i += kThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
     __syncthreads();
-    for (int base = 0; base < n; base += kThreads) {
-      const int j = base + threadIdx.x;
-      bool hit = false;
-      uint32_t bin = 0;
-      if (j < n) {
-        const uint32_t key = order_key(__ldg(s + j));
-        hit = (key & mask) == prefix;
-        bin = (key >> shift) & bmask;
-      }
-      const uint32_t active = __ballot_sync(0xffffffffu, hit);
-      if (hit) {
-        const uint32_t peers = __match_any_sync(active, bin);
-        if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-      }
-    }
+    for_row(s, n, [&](int, float x, bool in) { add_to_hist(sm.hist, order_key(x), in, mask, prefix, shift, bmask); });
     __syncthreads();
-    // bins are scanned from the top: find B with count(> B) < remaining <= count(>= B)
-    const int per = nb / kThreads > 0 ? nb / kThreads : 1;
-    int local = 0;
-    const int hi_bin = nb - 1 - threadIdx.x * per;  // this thread's bins: hi_bin down to hi_bin-per+1
-    if (threadIdx.x * per < nb)
-      for (int x = 0; x < per; ++x) local += hist[hi_bin - x];
-    int total;
-    const int before = block_exclusive_scan(threadIdx.x * per < nb ? local : 0, warp_tot, total);
-    if (threadIdx.x * per < nb && before < remaining && before + local >= remaining) {
-      int acc = before;
-      for (int x = 0; x < per; ++x) {
-        const int c = hist[hi_bin - x];
-        if (acc + c >= remaining) {
-          sel_bin = hi_bin - x;
-          sel_above = acc;
-          break;
-        }
-        acc += c;
-      }
-    }
-    __syncthreads();
-    const int bin = sel_bin;
-    remaining -= sel_above;
+    find_bin(sm, nb, remaining);
+    const int bin = sm.sel_bin;
+    remaining -= sm.sel_above;
     prefix |= static_cast<uint32_t>(bin) << shift;
     mask |= bmask << shift;
-    const bool exact = hist[bin] == remaining;  // every element of this bin is kept
+    const bool exact = sm.hist[bin] == remaining;
     __syncthreads();
     if (exact) break;
   }
-
-  // ---- ordered selection ----
   const int seg = (n + kThreads - 1) / kThreads;
-  const int lo = min(n, threadIdx.x * seg), hi = min(n, lo + seg);
+  const int lo = min(n, static_cast<int>(threadIdx.x) * seg), hi = min(n, lo + seg);
   int gt = 0, eq = 0;
   for (int j = lo; j < hi; ++j) {
     const uint32_t key = order_key(__ldg(s + j)) & mask;
@@ -139,9 +196,9 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     eq += key == prefix;
   }
   int tot;
-  const int eq_before = block_exclusive_scan(eq, warp_tot, tot);
+  const int eq_before = block_exclusive_scan(eq, sm.warp_tot, tot);
   const int eq_take = max(0, min(eq, remaining - eq_before));
-  const int out_before = block_exclusive_scan(gt + eq_take, warp_tot, tot);
+  const int out_before = block_exclusive_scan(gt + eq_take, sm.warp_tot, tot);
   int pos = out_before, eq_seen = 0;
   for (int j = lo; j < hi; ++j) {
     const uint32_t key = order_key(__ldg(s + j)) & mask;
@@ -154,6 +211,72 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
   }
 }
 
+__global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __restrict__ scores, int64_t stride,
+                                                        const int32_t* __restrict__ seq_lens,
+                                                        const int32_t* __restrict__ qsl, int batch, int tok_begin,
+                                                        int32_t* __restrict__ out) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const int row = blockIdx.x;
+  const int t = tok_begin + row;
+  const int b = seq_of_token(qsl, batch, t);
+  const int q0 = __ldg(qsl + b), n_q = __ldg(qsl + b + 1) - q0;
+  const int n = __ldg(seq_lens + b) - n_q + (t - q0) + 1;  // positions 0..p
+  const float* s = scores + static_cast<int64_t>(row) * stride;
+  int32_t* o = out + static_cast<int64_t>(row) * k;
+
+  if (n <= k) {
+    for (int i = threadIdx.x; i < k; i += kThreads) o[i] = i < n ? i : -1;
+    return;
+  }
+  if (k > kMaxK) {
+    topk_slow(sm, s, n, k, o);
+    return;
+  }
+  // ---- pass 1: histogram of the top 12 bits ----
+  for (int i = threadIdx.x; i < kBins; i += kThreads) sm.hist[i] = 0;
+  if (threadIdx.x == 0) {
+    sm.n_sel = 0;
+    sm.n_cand = 0;
+  }
+  __syncthreads();
+  for_row(s, n, [&](int, float x, bool in) { add_to_hist(sm.hist, order_key(x), in, 0u, 0u, 20, kBins - 1); });
+  __syncthreads();
+  find_bin(sm, kBins, k);
+  const uint32_t bin = static_cast<uint32_t>(sm.sel_bin);
+  const int above = sm.sel_above;
+  const int in_bin = sm.hist[bin];
+  if (in_bin > kCap) {
+    topk_slow(sm, s, n, k, o);
+    return;
+  }
+  // ---- pass 2: keep bins above, collect bin B ----
+  for_row(s, n, [&](int j, float x, bool in) {
+    const uint32_t key = order_key(x);
+    const uint32_t kb = key >> 20;
+    warp_append<int>(in && kb > bin, j, sm.sel, &sm.n_sel, kMaxK);
+    warp_append<unsigned long long>(in && kb == bin,
+                                    (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j), sm.cand,
+                                    &sm.n_cand, kCap);
+  });
+  __syncthreads();
+  // ---- exact winners of bin B: key descending, position ascending ----
+  int m = 1;
+  while (m < in_bin) m <<= 1;
+  for (int i = in_bin + threadIdx.x; i < m; i += kThreads) sm.cand[i] = 0ull;
+  __syncthreads();
+  bitonic_sort<unsigned long long, true>(sm.cand, m);
+  const int need = k - above;
+  for (int i = threadIdx.x; i < need; i += kThreads)
+    sm.sel[above + i] = static_cast<int>(~static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull));
+  int kp = 1;
+  while (kp < k) kp <<= 1;
+  for (int i = k + threadIdx.x; i < kp; i += kThreads) sm.sel[i] = 0x7FFFFFFF;
+  __syncthreads();
+  bitonic_sort<int, false>(sm.sel, kp);
+  for (int i = threadIdx.x; i < k; i += kThreads) o[i] = sm.sel[i];
+}
+
 }  // namespace
 
 smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
@@ -162,8 +285,16 @@ smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride,
   (void)err;
   const int rows = tok_end - tok_begin;
   if (rows <= 0) return SMLA_OK;
-  topk_kernel<<<rows, kThreads, 0, stream>>>(top_k, scores, scores_stride, seq_lens, query_start_loc, batch,
-                                             tok_begin, topk_idx);
+  const size_t smem = sizeof(TopkSmem);
+  static bool attr_set = false;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return SMLA_ERR_CUDA;
+    attr_set = true;
+  }
+  topk_kernel<<<rows, kThreads, smem, stream>>>(top_k, scores, scores_stride, seq_lens, query_start_loc, batch,
+                                                tok_begin, topk_idx);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
