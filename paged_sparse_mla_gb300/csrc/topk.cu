@@ -5,16 +5,18 @@
 // loop: kernels"] names a dedicated top-k path among the kernels that matter.
 //
 // One CTA per query row; scores map to order-preserving 32-bit keys (-0 folded
-// onto +0).  Fast path, two coalesced reads of the row:
-//   1. a 4096-bin histogram of the top 12 key bits (warp-aggregated shared
-//      memory increments) gives the bin B holding the k-th largest key;
-//   2. elements in bins above B are kept outright; elements of bin B are
-//      collected as 64-bit (key, ~position) pairs in shared memory.
-// A bitonic sort of the candidates (key descending, position ascending)
-// supplies the remaining winners, and a bitonic sort of the k kept positions
-// writes them in ascending order.  If bin B holds more candidates than shared
-// memory does, the row falls back to a radix select over all 32 key bits
-// (three histogram passes) and an index-ordered selection pass.
+// onto +0).  Fast path, one coalesced read of the row:
+//   1. an 8,192-element strided sample (runs of 4) is radix-selected in shared
+//      memory to a threshold T whose rank in the sample leaves a safety margin
+//      above k/n of the sample;
+//   2. every element with key >= T is collected as a 64-bit (key, ~position)
+//      pair in shared memory (warp-aggregated appends).
+// If at least k and at most the capacity were collected, a bitonic sort of the
+// candidates (key descending, position ascending) gives the exact top-k, and a
+// bitonic sort of the k kept positions writes them in ascending order.  Rows
+// with at most `capacity` positions take every position as a candidate.
+// Otherwise the row falls back to a radix select over all 32 key bits (three
+// histogram passes) and an index-ordered selection pass.
 #include "smla_internal.h"
 
 namespace smla {
@@ -24,6 +26,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;
 constexpr int kCap = 8192;     // candidate capacity of the fast path (power of two)
+constexpr int kSample = 8192;  // sample size for the threshold (runs of 4)
 constexpr int kMaxK = 4096;    // largest k of the fast path (power of two)
 
 struct TopkSmem {
@@ -233,42 +236,67 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     topk_slow(sm, s, n, k, o);
     return;
   }
-  // ---- pass 1: histogram of the top 12 bits ----
-  for (int i = threadIdx.x; i < kBins; i += kThreads) sm.hist[i] = 0;
+  // ---- threshold from a sample (skipped when every position fits) ----
+  uint32_t thr = 0;  // keep keys >= thr
+  if (n > kCap) {
+    // sample: kSample / 4 runs of 4 consecutive positions, evenly spread over the row
+    uint32_t* samp = reinterpret_cast<uint32_t*>(sm.cand);
+    const int runs = kSample / 4;
+    for (int i = threadIdx.x; i < runs; i += kThreads) {
+      const int j = static_cast<int>((static_cast<int64_t>(i) * (n - 4)) / (runs - 1));
+#pragma unroll
+      for (int x = 0; x < 4; ++x) samp[4 * i + x] = order_key(__ldg(s + j + x));
+    }
+    // rank of the threshold in the sample: expected rank of the k-th largest plus a margin
+    const int r = static_cast<int>((static_cast<int64_t>(k) * kSample + n - 1) / n);
+    const int want = min(kSample, r + 4 * static_cast<int>(sqrtf(static_cast<float>(r))) + 16);
+    // radix select of the want-th largest sample key
+    uint32_t prefix = 0, mask = 0;
+    int remaining = want;
+    const int shifts[3] = {20, 8, 0};
+    const int widths[3] = {12, 12, 8};
+    for (int pass = 0; pass < 3; ++pass) {
+      const int shift = shifts[pass];
+      const uint32_t bmask = (1u << widths[pass]) - 1u;
+      const int nb = 1 << widths[pass];
+      for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
+      __syncthreads();
+      for (int i = threadIdx.x; i < kSample; i += kThreads)
+        add_to_hist(sm.hist, samp[i], true, mask, prefix, shift, bmask);
+      __syncthreads();
+      find_bin(sm, nb, remaining);
+      remaining -= sm.sel_above;
+      prefix |= static_cast<uint32_t>(sm.sel_bin) << shift;
+      mask |= bmask << shift;
+      __syncthreads();
+    }
+    thr = prefix;
+  }
   if (threadIdx.x == 0) {
-    sm.n_sel = 0;
     sm.n_cand = 0;
   }
   __syncthreads();
-  for_row(s, n, [&](int, float x, bool in) { add_to_hist(sm.hist, order_key(x), in, 0u, 0u, 20, kBins - 1); });
-  __syncthreads();
-  find_bin(sm, kBins, k);
-  const uint32_t bin = static_cast<uint32_t>(sm.sel_bin);
-  const int above = sm.sel_above;
-  const int in_bin = sm.hist[bin];
-  if (in_bin > kCap) {
-    topk_slow(sm, s, n, k, o);
-    return;
-  }
-  // ---- pass 2: keep bins above, collect bin B ----
+  // ---- one pass: collect every key >= thr ----
   for_row(s, n, [&](int j, float x, bool in) {
     const uint32_t key = order_key(x);
-    const uint32_t kb = key >> 20;
-    warp_append<int>(in && kb > bin, j, sm.sel, &sm.n_sel, kMaxK);
-    warp_append<unsigned long long>(in && kb == bin,
+    warp_append<unsigned long long>(in && key >= thr,
                                     (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j), sm.cand,
                                     &sm.n_cand, kCap);
   });
   __syncthreads();
-  // ---- exact winners of bin B: key descending, position ascending ----
+  const int n_cand = sm.n_cand;
+  if (n_cand < k || n_cand > kCap) {  // the sample's guess missed: exact radix select
+    topk_slow(sm, s, n, k, o);
+    return;
+  }
+  // ---- exact top-k of the candidates: key descending, position ascending ----
   int m = 1;
-  while (m < in_bin) m <<= 1;
-  for (int i = in_bin + threadIdx.x; i < m; i += kThreads) sm.cand[i] = 0ull;
+  while (m < n_cand) m <<= 1;
+  for (int i = n_cand + threadIdx.x; i < m; i += kThreads) sm.cand[i] = 0ull;
   __syncthreads();
   bitonic_sort<unsigned long long, true>(sm.cand, m);
-  const int need = k - above;
-  for (int i = threadIdx.x; i < need; i += kThreads)
-    sm.sel[above + i] = static_cast<int>(~static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull));
+  for (int i = threadIdx.x; i < k; i += kThreads)
+    sm.sel[i] = static_cast<int>(~static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull));
   int kp = 1;
   while (kp < k) kp <<= 1;
   for (int i = k + threadIdx.x; i < kp; i += kThreads) sm.sel[i] = 0x7FFFFFFF;
