@@ -111,6 +111,23 @@ __device__ __forceinline__ uint4 load_bf16x8_padded(const uint16_t* src, int ava
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Producer unit -> (key, piece).  A warp's 32 consecutive units cover 8
+// consecutive keys x 4 consecutive pieces, with lane & 7 selecting the key: the
+// eight lanes of each quarter-warp then store the same piece of 8 consecutive
+// rows, which the 128-byte swizzle spreads over all 32 banks, and each key's 4
+// pieces (64 contiguous record bytes) are read by one warp instruction.
+__device__ __forceinline__ void latent_unit(int u, int parts, int& key, int& part) {
+  const int lane = u & 31, w = u >> 5;
+  const int pgroups = parts / 4;
+  key = 8 * (w / pgroups) + (lane & 7);
+  part = 4 * (w % pgroups) + (lane >> 3);
+}
+__device__ __forceinline__ void rope_unit(int ur, int& key, int& v) {
+  const int lane = ur & 31, w = ur >> 5;
+  key = 8 * (w >> 1) + (lane & 7);
+  v = 4 * (w & 1) + (lane >> 3);
+}
+
 // Loads for one batch of the producer unit stream (see the key-tile loop):
 // latent units fetch 16 E4M3 codes and their fp32 scale, rope units fetch 8
 // bf16 (zero padded past d_rope).  Masked keys (nullptr record) read as zero.
@@ -124,15 +141,17 @@ __device__ __forceinline__ void load_units(const uint8_t* const* rec, int u0, in
     val[b] = make_uint4(0, 0, 0, 0);
     sc[b] = 0.f;
     if (u < n_lat) {
-      const uint8_t* r = rec[u / parts];
-      const int part = u % parts;
+      int key, part;
+      latent_unit(u, parts, key, part);
+      const uint8_t* r = rec[key];
       if (r != nullptr) {
         val[b] = __ldg(reinterpret_cast<const uint4*>(r) + part);
         sc[b] = __ldg(reinterpret_cast<const float*>(r + DL) + (part * 16) / qtile);
       }
     } else if (u < n_units) {
-      const int ur = u - n_lat, v = ur % 8;
-      const uint8_t* r = rec[ur / 8];
+      int key, v;
+      rope_unit(u - n_lat, key, v);
+      const uint8_t* r = rec[key];
       if (r != nullptr && v * 8 < DR) {
         const uint8_t* src = r + DL + 4 * n_scales + v * 16;
         if (rope16 && v * 8 + 8 <= DR)
@@ -188,12 +207,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       mbar_init(&sm.tok_full[i], 1);
       mbar_init(&sm.tok_empty[i], 5);
     }
-    mbar_init(&sm.q_full, kProducerThreads);
+    mbar_init(&sm.q_full, kProducerThreads / 32);   // one arrive per producer warp
     mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.kv_full, kProducerThreads);
+    mbar_init(&sm.kv_full, kProducerThreads / 32);
     mbar_init(&sm.kv_empty, 1);
     mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 128);
+    mbar_init(&sm.p_full, 4);                        // one arrive per softmax warp
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
@@ -244,10 +263,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         *reinterpret_cast<uint4*>(&sm.q[c][sw128_off(h, v)]) = val;
       }
       fence_proxy_async();
-      mbar_arrive(&sm.q_full);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.q_full);
       // ---- key tiles ----
-      // Unit stream of one tile: units [0, 128*parts) are 16-code latent pieces
-      // (key r = u / parts), units [128*parts, 128*(parts+8)) are 16-byte rope pieces.
+      // Unit stream of one tile: units [0, 128*parts) are 16-code latent pieces,
+      // units [128*parts, 128*(parts+8)) are 16-byte rope pieces (see latent_unit).
       constexpr int n_lat = kTile * parts;
       constexpr int n_units = n_lat + kTile * 8;
       auto fill_rec = [&](int tile, int buf) {
@@ -293,7 +313,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
             const int u = base + ptid + b * kProducerThreads;
             if (u >= n_units) break;
             if (u < n_lat) {
-              const int r = u / parts, part = u % parts;
+              int r, part;
+              latent_unit(u, parts, r, part);
               uint4 o0, o1;
               dequant16(cur[b], csc[b], o0, o1);
               const int d0 = part * 16;
@@ -301,7 +322,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
               *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0)]) = o0;
               *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0 + 1)]) = o1;
             } else {
-              const int ur = u - n_lat, r = ur / 8, v = ur % 8;
+              int r, v;
+              rope_unit(u - n_lat, r, v);
               *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(r, v)]) = cur[b];
             }
           }
@@ -312,7 +334,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           }
         }
         fence_proxy_async();
-        mbar_arrive(&sm.kv_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.kv_full);
         named_bar_sync(2, kProducerThreads);  // next tile's addresses complete; this tile's reads done
       }
       if (!ok) break;
@@ -492,7 +515,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         }
         fence_proxy_async();
         tc_fence_before();
-        mbar_arrive(&sm.p_full);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.p_full);
       }
       if (!ok) break;
       // ---- end of token: row sums, normalisation, lse ----

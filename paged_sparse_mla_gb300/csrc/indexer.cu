@@ -13,14 +13,14 @@
 //   * the contraction is one FP8 tcgen05.mma per 32 key dims with the 128 keys
 //     of a tile as M (TMEM lane = key) and the group's query heads as N
 //     (<= 4 tokens x 64 heads = 256), accumulated in fp32 in tensor memory;
-//   * warps 0-7 (epilogue; warps w and w+4 share TMEM lanes 32*(w%4).. and
-//     split the group's tokens) read a key's row of head dot products from
-//     TMEM and reduce sum_h w * ReLU(.) per token in registers -- no
-//     cross-thread reduction -- then scale by s_I[j] and store the fp32 score;
-//   * warps 8-11 (producers) stream 128-key tiles of the indexer-key region of
+//   * warps 0-15 (epilogue; warp w reads TMEM lanes 32*(w%4).. for query token
+//     w/4 of the group) read a key's row of head dot products from TMEM and
+//     reduce sum_h w * ReLU(.) per token in registers -- no cross-thread
+//     reduction -- then scale by s_I[j] and store the fp32 score;
+//   * warps 16-19 (producers) stream 128-key tiles of the indexer-key region of
 //     each block through the block table with 16-byte cp.async into 128-byte
 //     swizzled stages (one warp per tile, four tiles in flight per CTA);
-//   * warp 12 issues the MMAs and owns the tensor-memory allocation.
+//   * warp 20 issues the MMAs and owns the tensor-memory allocation.
 #include "smla_internal.h"
 
 namespace smla {
@@ -30,17 +30,19 @@ constexpr int kTile = 128;         // keys per tile (MMA M)
 constexpr int kGroup = 4;          // query tokens per item (MMA N = kGroup * n_idx_heads)
 constexpr int kStages = 8;         // key-tile ring
 constexpr int kChunkTiles = 16;    // tiles per work item (2048 keys)
-constexpr int kEpiWarps = 8;       // two warps per TMEM sub-partition, splitting the group's tokens
+constexpr int kEpiWarps = 16;      // four warps per TMEM sub-partition, one query token each
 constexpr int kProducers = 4;      // producer warps
 constexpr int kMmaWarp = kEpiWarps + kProducers;
 constexpr int kThreads = 32 * (kEpiWarps + kProducers + 1);
 constexpr int kMaxN = 256;         // MMA N limit
+constexpr int kMaxSeqSmem = 1024;  // batches up to this size keep their metadata in shared memory
 
 struct __align__(1024) IdxSmem {
   uint8_t keys[kStages][kTile * 128];   // 16 KB per stage, 1024-aligned
   uint8_t q[2][kMaxN * 128];            // 32 KB per buffer
   float kscale[kStages][kTile];         // s_I of the tile's keys, loaded with the keys
-  float4 w[kGroup * 64 / 4];            // epilogue-owned weights of the current item
+  float4 w[2][kGroup * 64 / 4];         // weights of the item whose q is in q[i]
+  int seq_meta[2 * kMaxSeqSmem + 1];     // query_start_loc[0..B], then seq_lens[0..B)
   uint64_t key_full[kStages], key_empty[kStages];
   uint64_t q_full[2], q_empty[2];
   uint64_t acc_full[2], acc_empty[2];
@@ -76,20 +78,22 @@ struct IdxArgs {
   unsigned* err;
 };
 
-__device__ __forceinline__ Item decode_item(const IdxArgs& A, int item) {
+__device__ __forceinline__ Item decode_item(const IdxArgs& A, const int* meta, int item) {
   Item it;
   it.valid = 0;
   const int g = item % A.n_groups;
   const int rest = item / A.n_groups;
   const int b = rest % A.batch;
   const int c = rest / A.batch;
-  const int q0 = __ldg(A.qsl + b), q1 = __ldg(A.qsl + b + 1);
+  const bool in_smem = A.batch <= kMaxSeqSmem;
+  const int q0 = in_smem ? meta[b] : __ldg(A.qsl + b);
+  const int q1 = in_smem ? meta[b + 1] : __ldg(A.qsl + b + 1);
   const int r0 = max(q0, A.tok_begin), r1 = min(q1, A.tok_end);  // this call's rows of sequence b
   const int first = r0 + g * kGroup;
   if (first >= r1) return it;
   const int n_grp = min(kGroup, r1 - first);
   const int n_q = q1 - q0;
-  const int p_first = __ldg(A.seq_lens + b) - n_q + (first - q0);
+  const int p_first = (in_smem ? meta[A.batch + 1 + b] : __ldg(A.seq_lens + b)) - n_q + (first - q0);
   const int p_last = p_first + n_grp - 1;
   const int key_begin = c * kChunkTiles * kTile;
   if (p_last < 0 || key_begin > p_last) return it;
@@ -122,18 +126,22 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.key_full[s], 32);
+      mbar_init(&sm.key_full[s], 1);               // one arrive per producer warp
       mbar_init(&sm.key_empty[s], 1 + kEpiWarps);  // MMA done + every epilogue warp read the scales
     }
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&sm.q_full[i], 32);
-      mbar_init(&sm.q_empty[i], 1);
+      mbar_init(&sm.q_full[i], 1);
+      mbar_init(&sm.q_empty[i], 1 + kEpiWarps);  // MMA done + every epilogue warp done with the weights
       mbar_init(&sm.acc_full[i], 1);
-      mbar_init(&sm.acc_empty[i], 32 * kEpiWarps);
+      mbar_init(&sm.acc_empty[i], kEpiWarps);      // one arrive per epilogue warp
     }
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
     mbar_fence_init();
+  }
+  if (A.batch <= kMaxSeqSmem) {
+    for (int i = threadIdx.x; i <= A.batch; i += kThreads) sm.seq_meta[i] = __ldg(A.qsl + i);
+    for (int i = threadIdx.x; i < A.batch; i += kThreads) sm.seq_meta[A.batch + 1 + i] = __ldg(A.seq_lens + i);
   }
   if (warp == kMmaWarp) tmem_alloc(&sm.tmem_slot, 512);
   tc_fence_before();
@@ -156,7 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
     const int64_t layer_off = static_cast<int64_t>(A.layer) * A.L.layer_stride;
     uint32_t k = 0, nitem = 0;
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-      const Item it = decode_item(A, item);
+      const Item it = decode_item(A, sm.seq_meta, item);
       if (!it.valid) continue;
       const int32_t* bt = A.block_table + static_cast<int64_t>(it.b) * A.bt_stride;
       if (pw == 0) {
@@ -166,10 +174,14 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         const uint32_t qbase = smem_u32(sm.q[qb]);
         const uint8_t* qsrc = A.q_idx + static_cast<int64_t>(it.t0) * H * kD + ch * 16;
         for (int r = r0; r < rows; r += kRowStep) cp_async16(qbase + sw128_off(r, ch), qsrc + r * kD, 16);
+        // the group's weights (n_grp * H floats, contiguous rows of w) ride along with q
+        const float* wsrc = A.w + static_cast<int64_t>(it.t0) * H;
+        for (int i = lane; i < rows / 4; i += 32) cp_async16(smem_u32(&sm.w[qb][i]), wsrc + 4 * i, 16);
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async();
-        mbar_arrive(&sm.q_full[qb]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.q_full[qb]);
       }
       for (int tile = 0; tile < it.n_tiles; ++tile, ++k) {
         if (static_cast<int>(k % kProducers) != pw) continue;
@@ -206,7 +218,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         cp_async_commit();
         cp_async_wait<0>();
         fence_proxy_async();
-        mbar_arrive(&sm.key_full[s]);
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.key_full[s]);
       }
       ++nitem;
     }
@@ -216,7 +229,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       uint32_t k = 0, nitem = 0, a = 0;
       bool issued = false;
       for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-        const Item it = decode_item(A, item);
+        const Item it = decode_item(A, sm.seq_meta, item);
         if (!it.valid) continue;
         const int qb = nitem & 1;
         if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
@@ -252,19 +265,17 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       }
     }
   } else {
-    // ------------------------------ epilogue (warps 0-7) ------------------------------
+    // ------------------------------ epilogue (warps 0-15) ------------------------------
     const int row = (warp & 3) * 32 + lane;  // TMEM lane == key within the tile
-    const int half = warp >> 2;              // tokens half, half+2 of the group
+    const int tok = warp >> 2;               // query token of the group handled by this warp
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    uint32_t a = 0;
+    uint32_t a = 0, nitem = 0;
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-      const Item it = decode_item(A, item);
+      const Item it = decode_item(A, sm.seq_meta, item);
       if (!it.valid) continue;
-      named_bar_sync(1, 32 * kEpiWarps);
-      float* wf = reinterpret_cast<float*>(sm.w);
-      for (int i = threadIdx.x; i < it.n_grp * H; i += 32 * kEpiWarps)
-        wf[i] = __ldg(A.w + static_cast<int64_t>(it.t0) * H + i);
-      named_bar_sync(1, 32 * kEpiWarps);
+      const int qb = nitem & 1;
+      if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
+      const float4* wq = sm.w[qb];
       bool ok = true;
       for (int tile = 0; tile < it.n_tiles; ++tile, ++a) {
         const int j = it.key_begin + tile * kTile + row;
@@ -276,9 +287,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         tc_fence_after();
         const int st = a % kStages;  // the MMA consumed global tile a from stage a % kStages
         const float s_key = sm.kscale[st][row];
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.key_empty[st]);
-        for (int i = half; i < it.n_grp; i += 2) {
+        for (int i = tok; i < it.n_grp; i += kEpiWarps / 4) {
           float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
           for (int h0 = 0; h0 < H; h0 += 32) {
@@ -287,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
             tmem_ld_wait();
 #pragma unroll
             for (int x = 0; x < 32 && h0 + x < H; x += 4) {
-              const float4 wv = sm.w[(i * H + h0 + x) / 4];
+              const float4 wv = wq[(i * H + h0 + x) / 4];
               acc[0] = fmaf(fmaxf(__uint_as_float(v[x]), 0.f), wv.x, acc[0]);
               acc[1] = fmaf(fmaxf(__uint_as_float(v[x + 1]), 0.f), wv.y, acc[1]);
               acc[2] = fmaf(fmaxf(__uint_as_float(v[x + 2]), 0.f), wv.z, acc[2]);
@@ -300,9 +309,16 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
           }
         }
         tc_fence_before();
-        mbar_arrive(&sm.acc_empty[ab]);
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive_relaxed(&sm.acc_empty[ab]);   // TMEM reads are complete (wait::ld)
+          mbar_arrive_relaxed(&sm.key_empty[st]);   // the key scales were consumed above
+        }
       }
       if (!ok) break;
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&sm.q_empty[qb]);  // this warp is done with the item's weights
+      ++nitem;
     }
   }
 
