@@ -61,7 +61,8 @@ typedef enum smla_status {
   SMLA_ERR_UNSUPPORTED = 2,  /* shape not built into this library / no sm_103a device */
   SMLA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed       */
   SMLA_ERR_BAD_INDEX = 4,    /* device saw a block id / slot outside the pool (read clamped) */
-  SMLA_ERR_TIMEOUT = 5       /* a bounded on-device wait gave up            */
+  SMLA_ERR_TIMEOUT = 5,      /* a bounded on-device wait gave up            */
+  SMLA_ERR_SCRATCH_LIMIT = 6 /* smla_decode_static: one query token's scratch exceeds the static array */
 } smla_status_t;
 
 /*
@@ -200,6 +201,37 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
                           int batch, int n_tokens, int max_q, int max_ctx, void* out, float* lse,
                           int32_t* topk_idx_out, void* workspace, size_t workspace_bytes,
                           void* stream);
+
+/*
+ * smla_decode_static -- smla_decode for callers that cannot allocate device
+ * memory, such as code whose device memory is entirely owned by a serving
+ * engine's allocator (one that reserves all free HBM for the KV block pool and
+ * hands out no other buffers) or a host runtime with no device-allocation hook.
+ * The pages have no counterpart of this entry point; it only changes where the
+ * scratch lives.
+ *   Arguments and results are those of smla_decode without workspace /
+ *   workspace_bytes: the fp32 scores and top-k indices live in a 64 MiB static
+ *   __device__ array inside the library, which every GPU that loads the library
+ *   holds until the process exits.  No cudaMalloc/cudaFree or other allocating
+ *   call is made.
+ *   Query tokens are processed in groups that fit the array; if a single query
+ *   token needs more (4 * round_up(max_ctx, 4) + 4 * top_k bytes > 64 MiB - 512,
+ *   i.e. max_ctx above about 16.7M positions), the call returns
+ *   SMLA_ERR_SCRATCH_LIMIT before enqueuing anything.
+ *   The first call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) with that device current; make it before any stream
+ *   capture.  All calls share the array and it keeps the last call's contents
+ *   (nothing in it needs to start at zero); calls that overlap on the GPU race
+ *   on it, so order them on one stream.
+ */
+smla_status_t smla_decode_static(const smla_layout_t* layout, const smla_params_t* params, void* pool,
+                                 int layer, const void* new_latent, const void* new_rope,
+                                 const uint8_t* new_idx_k, const float* new_idx_scale,
+                                 const int64_t* slot_mapping, const void* q, const void* q_pe,
+                                 const uint8_t* q_idx, const float* w, const int32_t* block_table,
+                                 int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                                 int batch, int n_tokens, int max_q, int max_ctx, void* out, float* lse,
+                                 int32_t* topk_idx_out, void* stream);
 
 /* Synchronise `stream`, return the latched device error (and clear it). */
 smla_status_t smla_get_last_error(void* stream);

@@ -17,16 +17,17 @@ from . import build_lib
 __all__ = [
     "SmlaError", "Layout", "Params", "lib", "layout_init", "workspace_size", "kvpack_store",
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
-    "status_string", "version", "EXPORTED_SYMBOLS",
+    "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
+    "smla_decode_static",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
-          4: "SMLA_ERR_BAD_INDEX", 5: "SMLA_ERR_TIMEOUT"}
+          4: "SMLA_ERR_BAD_INDEX", 5: "SMLA_ERR_TIMEOUT", 6: "SMLA_ERR_SCRATCH_LIMIT"}
 
 
 class SmlaError(RuntimeError):
@@ -80,6 +81,8 @@ def lib() -> ctypes.CDLL:
             "smla_attend": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P]),
             "smla_decode": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I,
                                  _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "smla_decode_static": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
+                                        _I, _I, _I, _P, _P, _P, _P]),
             "smla_get_last_error": (_I, [_P]),
             "smla_status_string": (ctypes.c_char_p, [_I]),
             "smla_version": (_I, []),
@@ -197,6 +200,23 @@ def smla_decode(layout, params, pool, layer, new_latent, new_rope, new_idx_k, ne
                              _ptr(seq_lens), _ptr(query_start_loc), seq_lens.numel(), q.shape[0], max_q, max_ctx,
                              _ptr(out), _ptr(lse), _ptr(topk_idx_out), _ptr(workspace), workspace.numel(),
                              _stream(stream)), "smla_decode")
+
+
+def smla_decode_static(layout, params, pool, layer, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping,
+                       q, q_pe, q_idx, w, block_table, seq_lens, query_start_loc, max_q, max_ctx, out, lse,
+                       topk_idx_out=None, stream=None):
+    """smla_decode without a workspace argument, for callers that cannot allocate device memory.
+
+    The scores and top-k scratch live in the library's static 64 MiB device
+    array; calls share it, so calls that overlap on the GPU race on it.
+    """
+    _expect(q, torch.bfloat16, "q")
+    _check(lib().smla_decode_static(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(new_latent),
+                                    _ptr(new_rope), _ptr(new_idx_k), _ptr(new_idx_scale), _ptr(slot_mapping), _ptr(q),
+                                    _ptr(q_pe), _ptr(q_idx), _ptr(w), _ptr(block_table), block_table.shape[1],
+                                    _ptr(seq_lens), _ptr(query_start_loc), seq_lens.numel(), q.shape[0], max_q,
+                                    max_ctx, _ptr(out), _ptr(lse), _ptr(topk_idx_out), _stream(stream)),
+           "smla_decode_static")
 
 
 def smla_get_last_error(stream=None) -> int:

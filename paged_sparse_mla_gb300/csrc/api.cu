@@ -89,6 +89,7 @@ const char* smla_status_string(smla_status_t s) {
     case SMLA_ERR_CUDA: return "SMLA_ERR_CUDA";
     case SMLA_ERR_BAD_INDEX: return "SMLA_ERR_BAD_INDEX";
     case SMLA_ERR_TIMEOUT: return "SMLA_ERR_TIMEOUT";
+    case SMLA_ERR_SCRATCH_LIMIT: return "SMLA_ERR_SCRATCH_LIMIT";
   }
   return "SMLA_ERR_UNKNOWN";
 }
