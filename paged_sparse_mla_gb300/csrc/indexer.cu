@@ -43,6 +43,8 @@ struct __align__(1024) IdxSmem {
   float kscale[kStages][kTile];         // s_I of the tile's keys, loaded with the keys
   float4 w[2][kGroup * 64 / 4];         // weights of the item whose q is in q[i]
   int seq_meta[2 * kMaxSeqSmem + 1];     // query_start_loc[0..B], then seq_lens[0..B)
+  int item_off[kMaxSeqSmem + 1];         // first dense work item of each sequence (prefix sum)
+  int chunks[kMaxSeqSmem];               // key chunks of each sequence's last query group
   uint64_t key_full[kStages], key_empty[kStages];
   uint64_t q_full[2], q_empty[2];
   uint64_t acc_full[2], acc_empty[2];
@@ -109,6 +111,87 @@ __device__ __forceinline__ Item decode_item(const IdxArgs& A, const int* meta, i
   return it;
 }
 
+// Dense work items (batches up to kMaxSeqSmem): sequence b owns items
+// item_off[b] .. item_off[b+1]-1, enumerating (query group g, key chunk c) with
+// c fastest, c < chunks[b]; consecutive items are consecutive chunks, so the
+// CTAs running at the same time share sequences (and prefix-shared blocks).
+__device__ __forceinline__ Item decode_dense(const IdxArgs& A, const int* meta, const int* item_off,
+                                             const int* chunks, int item) {
+  int lo = 0, hi = A.batch - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (item_off[mid] <= item) lo = mid; else hi = mid - 1;
+  }
+  const int b = lo;
+  const int local = item - item_off[b];
+  const int nc = chunks[b];
+  const int g = local / nc, c = local % nc;
+  Item it;
+  it.valid = 0;
+  const int q0 = meta[b], q1 = meta[b + 1];
+  const int r0 = max(q0, A.tok_begin), r1 = min(q1, A.tok_end);
+  const int first = r0 + g * kGroup;
+  if (first >= r1) return it;
+  const int n_grp = min(kGroup, r1 - first);
+  const int p_first = meta[A.batch + 1 + b] - (q1 - q0) + (first - q0);
+  const int p_last = p_first + n_grp - 1;
+  const int key_begin = c * kChunkTiles * kTile;
+  if (p_last < 0 || key_begin > p_last) return it;  // an early group of a long chunk list
+  const int key_end = min(key_begin + kChunkTiles * kTile, p_last + 1);
+  it.valid = 1;
+  it.b = b;
+  it.t0 = first;
+  it.n_grp = n_grp;
+  it.p_first = p_first;
+  it.key_begin = key_begin;
+  it.key_end = key_end;
+  it.n_tiles = (key_end - key_begin + kTile - 1) / kTile;
+  return it;
+}
+
+// Items per sequence and their prefix sum (one warp).
+__device__ void build_item_table(const IdxArgs& A, const int* meta, int* item_off, int* chunks) {
+  const int lane = threadIdx.x & 31;
+  const int per = (A.batch + 31) / 32;
+  const int b0 = min(A.batch, lane * per), b1 = min(A.batch, b0 + per);
+  int local = 0;
+  for (int b = b0; b < b1; ++b) {
+    const int q0 = meta[b], q1 = meta[b + 1];
+    const int r0 = max(q0, A.tok_begin), r1 = min(q1, A.tok_end);
+    const int rows = max(0, r1 - r0);
+    const int p_last = meta[A.batch + 1 + b] - (q1 - q0) + (r1 - 1 - q0);
+    const int nc = (rows > 0 && p_last >= 0) ? (p_last + kChunkTiles * kTile) / (kChunkTiles * kTile) : 0;
+    chunks[b] = max(nc, 1);
+    local += ((rows + kGroup - 1) / kGroup) * nc;
+  }
+  int incl = local;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  int run = incl - local;
+  for (int b = b0; b < b1; ++b) {
+    item_off[b] = run;
+    const int q0 = meta[b], q1 = meta[b + 1];
+    const int rows = max(0, min(q1, A.tok_end) - max(q0, A.tok_begin));
+    const int p_last = meta[A.batch + 1 + b] - (q1 - q0) + (min(q1, A.tok_end) - 1 - q0);
+    const int nc = (rows > 0 && p_last >= 0) ? (p_last + kChunkTiles * kTile) / (kChunkTiles * kTile) : 0;
+    run += ((rows + kGroup - 1) / kGroup) * nc;
+  }
+  if (lane == 31) item_off[A.batch] = incl;
+}
+
+__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
+  unsigned long long d;
+  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
+      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
+      "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
+      : "=l"(d)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return make_float2(__uint_as_float(static_cast<uint32_t>(d)), __uint_as_float(static_cast<uint32_t>(d >> 32)));
+}
+
 __device__ __forceinline__ int mma_n(int n_grp, int heads) {
   const int n = n_grp * heads;
   return max(16, (n + 15) & ~15);
@@ -120,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
   IdxSmem& sm = *reinterpret_cast<IdxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int n_items = A.n_chunks * A.batch * A.n_groups;
+  const bool dense = A.batch <= kMaxSeqSmem;
   constexpr int H = kH;
   constexpr int D = kD;
 
@@ -139,9 +222,11 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
     sm.abort = 0;
     mbar_fence_init();
   }
-  if (A.batch <= kMaxSeqSmem) {
+  if (dense) {
     for (int i = threadIdx.x; i <= A.batch; i += kThreads) sm.seq_meta[i] = __ldg(A.qsl + i);
     for (int i = threadIdx.x; i < A.batch; i += kThreads) sm.seq_meta[A.batch + 1 + i] = __ldg(A.seq_lens + i);
+    __syncthreads();
+    if (warp == 0) build_item_table(A, sm.seq_meta, sm.item_off, sm.chunks);
   }
   if (warp == kMmaWarp) tmem_alloc(&sm.tmem_slot, 512);
   tc_fence_before();
@@ -149,6 +234,10 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
   volatile int* abort = &sm.abort;
+  const int n_items = dense ? sm.item_off[A.batch] : A.n_chunks * A.batch * A.n_groups;
+  const auto item_at = [&](int item) {
+    return dense ? decode_dense(A, sm.seq_meta, sm.item_off, sm.chunks, item) : decode_item(A, sm.seq_meta, item);
+  };
 
   if (warp >= kEpiWarps && warp < kMmaWarp) {
     // ------------------------------ producers ------------------------------
@@ -164,7 +253,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
     const int64_t layer_off = static_cast<int64_t>(A.layer) * A.L.layer_stride;
     uint32_t k = 0, nitem = 0;
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-      const Item it = decode_item(A, sm.seq_meta, item);
+      const Item it = item_at(item);
       if (!it.valid) continue;
       const int32_t* bt = A.block_table + static_cast<int64_t>(it.b) * A.bt_stride;
       if (pw == 0) {
@@ -229,7 +318,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       uint32_t k = 0, nitem = 0, a = 0;
       bool issued = false;
       for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-        const Item it = decode_item(A, sm.seq_meta, item);
+        const Item it = item_at(item);
         if (!it.valid) continue;
         const int qb = nitem & 1;
         if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
@@ -271,7 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     uint32_t a = 0, nitem = 0;
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-      const Item it = decode_item(A, sm.seq_meta, item);
+      const Item it = item_at(item);
       if (!it.valid) continue;
       const int qb = nitem & 1;
       if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
@@ -288,7 +377,8 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         const int st = a % kStages;  // the MMA consumed global tile a from stage a % kStages
         const float s_key = sm.kscale[st][row];
         for (int i = tok; i < it.n_grp; i += kEpiWarps / 4) {
-          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+          // two packed accumulator pairs: head h goes to lane h % 4 of (acc01, acc23)
+          float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
           for (int h0 = 0; h0 < H; h0 += 32) {
             uint32_t v[32];
@@ -297,13 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
 #pragma unroll
             for (int x = 0; x < 32 && h0 + x < H; x += 4) {
               const float4 wv = wq[(i * H + h0 + x) / 4];
-              acc[0] = fmaf(fmaxf(__uint_as_float(v[x]), 0.f), wv.x, acc[0]);
-              acc[1] = fmaf(fmaxf(__uint_as_float(v[x + 1]), 0.f), wv.y, acc[1]);
-              acc[2] = fmaf(fmaxf(__uint_as_float(v[x + 2]), 0.f), wv.z, acc[2]);
-              acc[3] = fmaf(fmaxf(__uint_as_float(v[x + 3]), 0.f), wv.w, acc[3]);
+              const float2 r01 = make_float2(fmaxf(__uint_as_float(v[x]), 0.f), fmaxf(__uint_as_float(v[x + 1]), 0.f));
+              const float2 r23 =
+                  make_float2(fmaxf(__uint_as_float(v[x + 2]), 0.f), fmaxf(__uint_as_float(v[x + 3]), 0.f));
+              acc01 = ffma2(r01, make_float2(wv.x, wv.y), acc01);
+              acc23 = ffma2(r23, make_float2(wv.z, wv.w), acc23);
             }
           }
-          const float total = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+          const float total = (acc01.x + acc01.y) + (acc23.x + acc23.y);
           if (j <= it.p_first + i && j < it.key_end) {
             A.scores[static_cast<int64_t>(it.t0 + i - A.tok_begin) * A.scores_stride + j] = total * s_key;
           }

@@ -10,10 +10,12 @@
 //      memory to a threshold T whose rank in the sample leaves a safety margin
 //      above k/n of the sample;
 //   2. every element with key >= T is collected as a 64-bit (key, ~position)
-//      pair in shared memory (warp-aggregated appends).
-// If at least k and at most the capacity were collected, a bitonic sort of the
-// candidates (key descending, position ascending) gives the exact top-k, and a
-// bitonic sort of the k kept positions writes them in ascending order.  Rows
+//      pair in shared memory (warp-aggregated appends, four 16-byte loads in
+//      flight per thread).
+// If at least k and at most the capacity were collected, a radix select over the
+// candidates gives the exact k-th largest key; keys above it are kept, ties keep
+// their lowest positions, and a bitonic sort of the k kept positions writes
+// them in ascending order.  Rows
 // with at most `capacity` positions take every position as a candidate.
 // Otherwise the row falls back to a radix select over all 32 key bits (three
 // histogram passes) and an index-ordered selection pass.
@@ -34,7 +36,7 @@ struct TopkSmem {
   unsigned long long cand[kCap];
   int sel[kMaxK];
   int warp_tot[32];
-  int n_sel, n_cand, sel_bin, sel_above;
+  int n_sel, n_cand, n_tie, sel_bin, sel_above;
 };
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -168,6 +170,63 @@ __device__ __forceinline__ void warp_append(bool pred, T v, T* list, int* counte
   }
 }
 
+// The want-th largest of n keys in shared memory (radix select on 12, 12, 8
+// bits).  `rem` returns how many keys equal to the result are within the top
+// `want` (1 <= rem <= count of that key).
+__device__ uint32_t radix_select(TopkSmem& sm, const uint32_t* keys, int n, int want, int& rem) {
+  uint32_t prefix = 0, mask = 0;
+  int remaining = want;
+  const int shifts[3] = {20, 8, 0};
+  const int widths[3] = {12, 12, 8};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass];
+    const uint32_t bmask = (1u << widths[pass]) - 1u;
+    const int nb = 1 << widths[pass];
+    for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kThreads) {
+      const int i = base + threadIdx.x;
+      add_to_hist(sm.hist, i < n ? keys[i] : 0u, i < n, mask, prefix, shift, bmask);
+    }
+    __syncthreads();
+    find_bin(sm, nb, remaining);
+    remaining -= sm.sel_above;
+    prefix |= static_cast<uint32_t>(sm.sel_bin) << shift;
+    mask |= bmask << shift;
+    __syncthreads();
+  }
+  rem = remaining;
+  return prefix;
+}
+
+// The k-th largest key among the packed (key << 32 | ~position) candidates.
+__device__ uint32_t radix_select_cand(TopkSmem& sm, int n, int k, int& rem) {
+  uint32_t prefix = 0, mask = 0;
+  int remaining = k;
+  const int shifts[3] = {20, 8, 0};
+  const int widths[3] = {12, 12, 8};
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = shifts[pass];
+    const uint32_t bmask = (1u << widths[pass]) - 1u;
+    const int nb = 1 << widths[pass];
+    for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
+    __syncthreads();
+    for (int base = 0; base < n; base += kThreads) {
+      const int i = base + threadIdx.x;
+      const uint32_t key = i < n ? static_cast<uint32_t>(sm.cand[i] >> 32) : 0u;
+      add_to_hist(sm.hist, key, i < n, mask, prefix, shift, bmask);
+    }
+    __syncthreads();
+    find_bin(sm, nb, remaining);
+    remaining -= sm.sel_above;
+    prefix |= static_cast<uint32_t>(sm.sel_bin) << shift;
+    mask |= bmask << shift;
+    __syncthreads();
+  }
+  rem = remaining;
+  return prefix;
+}
+
 __device__ void topk_slow(TopkSmem& sm, const float* s, int n, int k, int32_t* o) {
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
@@ -242,6 +301,7 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     // sample: kSample / 4 runs of 4 consecutive positions, evenly spread over the row
     uint32_t* samp = reinterpret_cast<uint32_t*>(sm.cand);
     const int runs = kSample / 4;
+#pragma unroll 4
     for (int i = threadIdx.x; i < runs; i += kThreads) {
       const int j = static_cast<int>((static_cast<int64_t>(i) * (n - 4)) / (runs - 1));
 #pragma unroll
@@ -250,53 +310,96 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     // rank of the threshold in the sample: expected rank of the k-th largest plus a margin
     const int r = static_cast<int>((static_cast<int64_t>(k) * kSample + n - 1) / n);
     const int want = min(kSample, r + 4 * static_cast<int>(sqrtf(static_cast<float>(r))) + 16);
-    // radix select of the want-th largest sample key
-    uint32_t prefix = 0, mask = 0;
-    int remaining = want;
-    const int shifts[3] = {20, 8, 0};
-    const int widths[3] = {12, 12, 8};
-    for (int pass = 0; pass < 3; ++pass) {
-      const int shift = shifts[pass];
-      const uint32_t bmask = (1u << widths[pass]) - 1u;
-      const int nb = 1 << widths[pass];
-      for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
-      __syncthreads();
-      for (int i = threadIdx.x; i < kSample; i += kThreads)
-        add_to_hist(sm.hist, samp[i], true, mask, prefix, shift, bmask);
-      __syncthreads();
-      find_bin(sm, nb, remaining);
-      remaining -= sm.sel_above;
-      prefix |= static_cast<uint32_t>(sm.sel_bin) << shift;
-      mask |= bmask << shift;
-      __syncthreads();
-    }
-    thr = prefix;
+    __syncthreads();
+    int rem;
+    thr = radix_select(sm, samp, kSample, want, rem);
   }
-  if (threadIdx.x == 0) {
-    sm.n_cand = 0;
-  }
+  if (threadIdx.x == 0) sm.n_cand = 0;
   __syncthreads();
-  // ---- one pass: collect every key >= thr ----
-  for_row(s, n, [&](int j, float x, bool in) {
+  // ---- one pass: collect every key >= thr (four 16-byte loads in flight per thread) ----
+  const auto collect = [&](int j, float x, bool in) {
     const uint32_t key = order_key(x);
     warp_append<unsigned long long>(in && key >= thr,
                                     (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j), sm.cand,
                                     &sm.n_cand, kCap);
-  });
+  };
+  if ((reinterpret_cast<uintptr_t>(s) & 15) == 0) {
+    constexpr int U = 4;
+    const int n4 = (n + 3) / 4;
+    const int span = kThreads * U;
+    const int bound = (n4 + span - 1) / span * span;
+    for (int base = threadIdx.x; base < bound; base += span) {
+      float4 v[U];
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = 4 * (base + u * kThreads);
+        if (j + 3 < n) {
+          v[u] = __ldg(reinterpret_cast<const float4*>(s + j));
+        } else {
+          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+          if (j < n) v[u].x = __ldg(s + j);
+          if (j + 1 < n) v[u].y = __ldg(s + j + 1);
+          if (j + 2 < n) v[u].z = __ldg(s + j + 2);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int j = 4 * (base + u * kThreads);
+        const bool hit = (j < n && order_key(v[u].x) >= thr) || (j + 1 < n && order_key(v[u].y) >= thr) ||
+                         (j + 2 < n && order_key(v[u].z) >= thr) || (j + 3 < n && order_key(v[u].w) >= thr);
+        if (__any_sync(0xffffffffu, hit)) {
+          collect(j, v[u].x, j < n);
+          collect(j + 1, v[u].y, j + 1 < n);
+          collect(j + 2, v[u].z, j + 2 < n);
+          collect(j + 3, v[u].w, j + 3 < n);
+        }
+      }
+    }
+  } else {
+    for_row(s, n, collect);
+  }
   __syncthreads();
   const int n_cand = sm.n_cand;
-  if (n_cand < k || n_cand > kCap) {  // the sample's guess missed: exact radix select
+  if (n_cand < k || n_cand > kCap) {  // the sample's guess missed: exact radix select over the row
     topk_slow(sm, s, n, k, o);
     return;
   }
-  // ---- exact top-k of the candidates: key descending, position ascending ----
-  int m = 1;
-  while (m < n_cand) m <<= 1;
-  for (int i = n_cand + threadIdx.x; i < m; i += kThreads) sm.cand[i] = 0ull;
+  // ---- exact k-th largest key T among the candidates, and how many keys == T to keep ----
+  int need_eq;
+  const uint32_t T = radix_select_cand(sm, n_cand, k, need_eq);
+  // ---- keep key > T, and the need_eq lowest positions among key == T ----
+  if (threadIdx.x == 0) {
+    sm.n_sel = 0;
+    sm.n_tie = 0;
+  }
   __syncthreads();
-  bitonic_sort<unsigned long long, true>(sm.cand, m);
-  for (int i = threadIdx.x; i < k; i += kThreads)
-    sm.sel[i] = static_cast<int>(~static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull));
+  int* ties = sm.hist;  // free after the radix passes
+  for (int base = 0; base < n_cand; base += kThreads) {
+    const int i = base + threadIdx.x;
+    uint32_t key = 0;
+    int j = 0;
+    if (i < n_cand) {
+      key = static_cast<uint32_t>(sm.cand[i] >> 32);
+      j = static_cast<int>(~static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull));
+    }
+    warp_append<int>(i < n_cand && key > T, j, sm.sel, &sm.n_sel, kMaxK);
+    warp_append<int>(i < n_cand && key == T, j, ties, &sm.n_tie, kBins);
+  }
+  __syncthreads();
+  const int n_tie = sm.n_tie;
+  if (n_tie > kBins) {  // more equal keys than the tie buffer holds
+    topk_slow(sm, s, n, k, o);
+    return;
+  }
+  if (n_tie > need_eq) {  // keep the lowest positions among the ties
+    int mt = 1;
+    while (mt < n_tie) mt <<= 1;
+    for (int i = n_tie + threadIdx.x; i < mt; i += kThreads) ties[i] = 0x7FFFFFFF;
+    __syncthreads();
+    bitonic_sort<int, false>(ties, mt);
+  }
+  const int gt = sm.n_sel;
+  for (int i = threadIdx.x; i < need_eq; i += kThreads) sm.sel[gt + i] = ties[i];
   int kp = 1;
   while (kp < k) kp <<= 1;
   for (int i = k + threadIdx.x; i < kp; i += kThreads) sm.sel[i] = 0x7FFFFFFF;
