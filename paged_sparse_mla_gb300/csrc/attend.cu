@@ -60,7 +60,6 @@ struct __align__(1024) AttnSmem {
   uint64_t q_full, q_empty, kv_full, kv_empty, s_full, p_full, o_done, final_bar;
   uint32_t tmem_slot;
   int abort;
-  int rescale;
 };
 
 struct AttnArgs {
@@ -97,6 +96,25 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[kHeads], int la
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
+}
+
+// 2^x with the hardware approximation (MUFU; relative error ~2^-22, -inf -> 0).
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Barrier over `n` threads (named barrier `id`) that returns the OR of `pred`.
+__device__ __forceinline__ int bar_red_or(int id, int n, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(n)
+      : "memory");
+  return r;
 }
 
 // Eight bf16 values from 2-byte aligned memory; entries at or beyond `avail` read as zero.
@@ -180,11 +198,24 @@ __device__ __forceinline__ void dequant16(const uint4& codes, float sc, uint4& o
   o1 = make_uint4(ow[4], ow[5], ow[6], ow[7]);
 }
 
-// Number of 128-key tiles a row needs: one past the last valid entry.
+// Number of 128-key tiles a row needs: one past the last valid entry.  A row
+// whose final entry is valid needs every tile (one load); otherwise the warp
+// scans the row with all of its loads in flight at once.
 __device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
+  if (__ldg(row + k - 1) >= 0) return (k + kTile - 1) / kTile;
   int last = -1;
-  for (int i = lane; i < k; i += 32)
-    if (__ldg(row + i) >= 0) last = i;
+  constexpr int kUnroll = 8;
+  for (int base = 0; base < k; base += 32 * kUnroll) {
+    int v[kUnroll];
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x) {
+      const int i = base + x * 32 + lane;
+      v[x] = i < k ? __ldg(row + i) : -1;
+    }
+#pragma unroll
+    for (int x = 0; x < kUnroll; ++x)
+      if (v[x] >= 0) last = max(last, base + x * 32 + lane);
+  }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) last = max(last, __shfl_xor_sync(0xffffffffu, last, o));
   return (last + kTile) / kTile;
@@ -248,6 +279,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       const int32_t* bt = A.block_table + static_cast<int64_t>(b) * A.bt_stride;
       // ---- query -> swizzled bf16 chunks (heads and rope dims zero padded) ----
       if (!mbar_wait(&sm.q_empty, (nw & 1) ^ 1, A.err, abort)) break;
+#pragma unroll 4
       for (int u = ptid; u < kHeads * NCH * 8; u += kProducerThreads) {
         const int h = u / (NCH * 8), rem = u % (NCH * 8), c = rem / 8, v = rem % 8;
         uint4 val = make_uint4(0, 0, 0, 0);
@@ -444,22 +476,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           sm.red[warp][2 * lane + 1] = v[1];
         }
         named_bar_sync(1, 128);
+        int need_h = 0;
         if (tid < kHeads) {
           const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
           sm.m_tile[tid] = mt;
+          need_h = tile == 0 || mt > sm.m_run[tid] + kRescaleThreshold;
         }
-        named_bar_sync(1, 128);
-        if (tid == 0) {
-          int need = 0;
-          if (tile == 0) {
-            need = 1;
-          } else {
-            for (int h = 0; h < kHeads; ++h) need |= sm.m_tile[h] > sm.m_run[h] + kRescaleThreshold;
-          }
-          sm.rescale = need;
-        }
-        named_bar_sync(1, 128);
-        if (sm.rescale) {
+        // one barrier that also ORs the per-head "running max must move" flags
+        if (bar_red_or(1, 128, need_h)) {
           if (tid < kHeads) {
             const float old = tile == 0 ? -INFINITY : sm.m_run[tid];
             const float mn = fmaxf(old, sm.m_tile[tid]);
@@ -499,8 +523,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
             const float m0 = sm.m_run[h], m1 = sm.m_run[h + 1];
             const float s0 = valid ? __uint_as_float(r[hx]) * A.scale_log2 : -INFINITY;
             const float s1 = valid ? __uint_as_float(r[hx + 1]) * A.scale_log2 : -INFINITY;
-            const float p0 = exp2f(s0 - (m0 == -INFINITY ? 0.f : m0));
-            const float p1 = exp2f(s1 - (m1 == -INFINITY ? 0.f : m1));
+            const float p0 = fast_exp2(s0 - (m0 == -INFINITY ? 0.f : m0));
+            const float p1 = fast_exp2(s1 - (m1 == -INFINITY ? 0.f : m1));
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             const float2 pf = __bfloat1622float2(pb);
             l_part[h] += pf.x;
