@@ -7,20 +7,30 @@
 //   I[t, j] = s_I[j] * sum_h w[t, h] * ReLU(q_I[t, h] . k_I[j])
 //
 // Design (sm_103a, one persistent CTA per SM):
-//   * a work item is (key chunk c, sequence b, group g of <= 4 query tokens of b);
-//     items are ordered chunk-major so CTAs working at the same time read the
-//     same key chunk of neighbouring sequences (prefix-shared blocks hit L2);
+//   * a work item is (sequence b, group g of <= 4 query tokens of b, key chunk c
+//     of 2048 keys); the valid items are enumerated densely (prefix sums over
+//     the sequences, in shared memory) and dealt round-robin to the CTAs, so
+//     every CTA gets the same number of tiles to within one item, and CTAs that
+//     run at the same time work on neighbouring sequences (prefix-shared blocks
+//     are read once from HBM and then from L2);
 //   * the contraction is one FP8 tcgen05.mma per 32 key dims with the 128 keys
 //     of a tile as M (TMEM lane = key) and the group's query heads as N
-//     (<= 4 tokens x 64 heads = 256), accumulated in fp32 in tensor memory;
+//     (<= 4 tokens x 64 heads = 256), accumulated in fp32 in tensor memory,
+//     double-buffered;
 //   * warps 0-15 (epilogue; warp w reads TMEM lanes 32*(w%4).. for query token
-//     w/4 of the group) read a key's row of head dot products from TMEM and
-//     reduce sum_h w * ReLU(.) per token in registers -- no cross-thread
+//     w/4) hold their token's head weights in registers for the whole item and
+//     reduce sum_h w * ReLU(.) per key in registers -- no cross-thread
 //     reduction -- then scale by s_I[j] and store the fp32 score;
-//   * warps 16-19 (producers) stream 128-key tiles of the indexer-key region of
-//     each block through the block table with 16-byte cp.async into 128-byte
-//     swizzled stages (one warp per tile, four tiles in flight per CTA);
-//   * warp 20 issues the MMAs and owns the tensor-memory allocation.
+//   * warp 16 (producer) moves data with the tensor-memory-access unit: one 3-D
+//     tensor-map load per block of the indexer-key region (block ids from the
+//     block table, the MMA's swizzle applied by the copy, blocks beyond the
+//     context loaded out of bounds as zeros), a bulk copy of the block's key
+//     scales, and per item a 2-D tensor-map load of the group's query rows and a
+//     bulk copy of its weights; completion is counted in transaction bytes on
+//     the stage's mbarrier;
+//   * warp 17 issues the MMAs and owns the tensor-memory allocation.
+#include <cuda.h>
+
 #include "smla_internal.h"
 
 namespace smla {
@@ -31,11 +41,11 @@ constexpr int kGroup = 4;          // query tokens per item (MMA N = kGroup * n_
 constexpr int kStages = 8;         // key-tile ring
 constexpr int kChunkTiles = 16;    // tiles per work item (2048 keys)
 constexpr int kEpiWarps = 16;      // four warps per TMEM sub-partition, one query token each
-constexpr int kProducers = 4;      // producer warps
-constexpr int kMmaWarp = kEpiWarps + kProducers;
-constexpr int kThreads = 32 * (kEpiWarps + kProducers + 1);
+constexpr int kProducerWarp = kEpiWarps;
+constexpr int kMmaWarp = kEpiWarps + 1;
+constexpr int kThreads = 32 * (kEpiWarps + 2);
 constexpr int kMaxN = 256;         // MMA N limit
-constexpr int kMaxSeqSmem = 1024;  // batches up to this size keep their metadata in shared memory
+constexpr int kMaxSeqSmem = 1024;  // batches up to this size are scheduled densely
 
 struct __align__(1024) IdxSmem {
   uint8_t keys[kStages][kTile * 128];   // 16 KB per stage, 1024-aligned
@@ -68,7 +78,6 @@ struct IdxArgs {
   KernelLayout L;
   int n_idx_heads, layer;
   const uint8_t* pool;
-  const uint8_t* q_idx;
   const float* w;
   const int32_t* block_table;
   int bt_stride;
@@ -80,22 +89,61 @@ struct IdxArgs {
   unsigned* err;
 };
 
-__device__ __forceinline__ Item decode_item(const IdxArgs& A, const int* meta, int item) {
+// ---------------------------------------------------------------------------
+// Tensor-memory-access (TMA) and bulk-copy helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(map), "r"(x), "r"(y), "r"(z), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          dst),
+      "l"(map), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+
+// Shared-memory matrix descriptor for K-major rows of kD bytes: the 128-byte
+// swizzle for 128-byte rows, the 32-byte swizzle for 32-byte rows; 8-row groups.
+template <int kD>
+__device__ __forceinline__ uint64_t key_desc(uint32_t addr) {
+  if constexpr (kD == 128) {
+    return sw128_desc(addr, 16, 1024);
+  } else {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((addr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>(1) << 16;              // leading offset (unused for swizzled K-major)
+    d |= static_cast<uint64_t>((8 * kD) >> 4) << 32;  // 8 rows of kD bytes
+    d |= static_cast<uint64_t>(1) << 46;              // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(6) << 61;              // 32-byte swizzle
+    return d;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Work items
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ Item make_item(const IdxArgs& A, int b, int g, int c, int q0, int q1, int len_b) {
   Item it;
   it.valid = 0;
-  const int g = item % A.n_groups;
-  const int rest = item / A.n_groups;
-  const int b = rest % A.batch;
-  const int c = rest / A.batch;
-  const bool in_smem = A.batch <= kMaxSeqSmem;
-  const int q0 = in_smem ? meta[b] : __ldg(A.qsl + b);
-  const int q1 = in_smem ? meta[b + 1] : __ldg(A.qsl + b + 1);
   const int r0 = max(q0, A.tok_begin), r1 = min(q1, A.tok_end);  // this call's rows of sequence b
   const int first = r0 + g * kGroup;
   if (first >= r1) return it;
   const int n_grp = min(kGroup, r1 - first);
-  const int n_q = q1 - q0;
-  const int p_first = (in_smem ? meta[A.batch + 1 + b] : __ldg(A.seq_lens + b)) - n_q + (first - q0);
+  const int p_first = len_b - (q1 - q0) + (first - q0);
   const int p_last = p_first + n_grp - 1;
   const int key_begin = c * kChunkTiles * kTile;
   if (p_last < 0 || key_begin > p_last) return it;
@@ -111,58 +159,48 @@ __device__ __forceinline__ Item decode_item(const IdxArgs& A, const int* meta, i
   return it;
 }
 
-// Dense work items (batches up to kMaxSeqSmem): sequence b owns items
-// item_off[b] .. item_off[b+1]-1, enumerating (query group g, key chunk c) with
-// c fastest, c < chunks[b]; consecutive items are consecutive chunks, so the
-// CTAs running at the same time share sequences (and prefix-shared blocks).
-__device__ __forceinline__ Item decode_dense(const IdxArgs& A, const int* meta, const int* item_off,
-                                             const int* chunks, int item) {
+// Sparse enumeration for large batches: item = (c * batch + b) * n_groups + g.
+__device__ __forceinline__ Item decode_sparse(const IdxArgs& A, int item) {
+  const int g = item % A.n_groups;
+  const int rest = item / A.n_groups;
+  const int b = rest % A.batch;
+  const int c = rest / A.batch;
+  return make_item(A, b, g, c, __ldg(A.qsl + b), __ldg(A.qsl + b + 1), __ldg(A.seq_lens + b));
+}
+
+// Dense enumeration (batches up to kMaxSeqSmem): sequence b owns items
+// item_off[b] .. item_off[b+1]-1 = (group g, chunk c), c fastest, c < chunks[b].
+__device__ __forceinline__ Item decode_dense(const IdxArgs& A, const IdxSmem& sm, int item) {
   int lo = 0, hi = A.batch - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (item_off[mid] <= item) lo = mid; else hi = mid - 1;
+    if (sm.item_off[mid] <= item) lo = mid; else hi = mid - 1;
   }
   const int b = lo;
-  const int local = item - item_off[b];
-  const int nc = chunks[b];
-  const int g = local / nc, c = local % nc;
-  Item it;
-  it.valid = 0;
+  const int local = item - sm.item_off[b];
+  const int nc = sm.chunks[b];
+  return make_item(A, b, local / nc, local % nc, sm.seq_meta[b], sm.seq_meta[b + 1], sm.seq_meta[A.batch + 1 + b]);
+}
+
+__device__ __forceinline__ int seq_items(const IdxArgs& A, const int* meta, int b, int& nc) {
   const int q0 = meta[b], q1 = meta[b + 1];
   const int r0 = max(q0, A.tok_begin), r1 = min(q1, A.tok_end);
-  const int first = r0 + g * kGroup;
-  if (first >= r1) return it;
-  const int n_grp = min(kGroup, r1 - first);
-  const int p_first = meta[A.batch + 1 + b] - (q1 - q0) + (first - q0);
-  const int p_last = p_first + n_grp - 1;
-  const int key_begin = c * kChunkTiles * kTile;
-  if (p_last < 0 || key_begin > p_last) return it;  // an early group of a long chunk list
-  const int key_end = min(key_begin + kChunkTiles * kTile, p_last + 1);
-  it.valid = 1;
-  it.b = b;
-  it.t0 = first;
-  it.n_grp = n_grp;
-  it.p_first = p_first;
-  it.key_begin = key_begin;
-  it.key_end = key_end;
-  it.n_tiles = (key_end - key_begin + kTile - 1) / kTile;
-  return it;
+  const int rows = max(0, r1 - r0);
+  const int p_last = meta[A.batch + 1 + b] - (q1 - q0) + (r1 - 1 - q0);
+  nc = (rows > 0 && p_last >= 0) ? (p_last + kChunkTiles * kTile) / (kChunkTiles * kTile) : 0;
+  return ((rows + kGroup - 1) / kGroup) * nc;
 }
 
 // Items per sequence and their prefix sum (one warp).
-__device__ void build_item_table(const IdxArgs& A, const int* meta, int* item_off, int* chunks) {
+__device__ void build_item_table(const IdxArgs& A, IdxSmem& sm) {
   const int lane = threadIdx.x & 31;
   const int per = (A.batch + 31) / 32;
   const int b0 = min(A.batch, lane * per), b1 = min(A.batch, b0 + per);
   int local = 0;
   for (int b = b0; b < b1; ++b) {
-    const int q0 = meta[b], q1 = meta[b + 1];
-    const int r0 = max(q0, A.tok_begin), r1 = min(q1, A.tok_end);
-    const int rows = max(0, r1 - r0);
-    const int p_last = meta[A.batch + 1 + b] - (q1 - q0) + (r1 - 1 - q0);
-    const int nc = (rows > 0 && p_last >= 0) ? (p_last + kChunkTiles * kTile) / (kChunkTiles * kTile) : 0;
-    chunks[b] = max(nc, 1);
-    local += ((rows + kGroup - 1) / kGroup) * nc;
+    int nc;
+    local += seq_items(A, sm.seq_meta, b, nc);
+    sm.chunks[b] = max(nc, 1);
   }
   int incl = local;
 #pragma unroll
@@ -172,14 +210,11 @@ __device__ void build_item_table(const IdxArgs& A, const int* meta, int* item_of
   }
   int run = incl - local;
   for (int b = b0; b < b1; ++b) {
-    item_off[b] = run;
-    const int q0 = meta[b], q1 = meta[b + 1];
-    const int rows = max(0, min(q1, A.tok_end) - max(q0, A.tok_begin));
-    const int p_last = meta[A.batch + 1 + b] - (q1 - q0) + (min(q1, A.tok_end) - 1 - q0);
-    const int nc = (rows > 0 && p_last >= 0) ? (p_last + kChunkTiles * kTile) / (kChunkTiles * kTile) : 0;
-    run += ((rows + kGroup - 1) / kGroup) * nc;
+    sm.item_off[b] = run;
+    int nc;
+    run += seq_items(A, sm.seq_meta, b, nc);
   }
-  if (lane == 31) item_off[A.batch] = incl;
+  if (lane == 31) sm.item_off[A.batch] = incl;
 }
 
 __device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
@@ -198,23 +233,27 @@ __device__ __forceinline__ int mma_n(int n_grp, int heads) {
 }
 
 template <int kH, int kD, int kBS>
-__global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs A) {
+__global__ void __launch_bounds__(kThreads, 1)
+    index_scores_kernel(const IdxArgs A, const __grid_constant__ CUtensorMap key_map,
+                        const __grid_constant__ CUtensorMap q_map) {
   extern __shared__ uint8_t smem_raw[];
   IdxSmem& sm = *reinterpret_cast<IdxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const bool dense = A.batch <= kMaxSeqSmem;
   constexpr int H = kH;
-  constexpr int D = kD;
+  constexpr int kBlocks = kTile / kBS;  // blocks per tile
+  static_assert(kTile % kBS == 0 && kBlocks <= 32 && kBS % 4 == 0, "tile geometry");
+  static_assert(H % 4 == 0 && H * kGroup <= kMaxN, "head geometry");
+  const bool dense = A.batch <= kMaxSeqSmem;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < kStages; ++s) {
-      mbar_init(&sm.key_full[s], 1);               // one arrive per producer warp
+      mbar_init(&sm.key_full[s], 1);               // producer arrive + transaction bytes
       mbar_init(&sm.key_empty[s], 1 + kEpiWarps);  // MMA done + every epilogue warp read the scales
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.q_full[i], 1);
-      mbar_init(&sm.q_empty[i], 1 + kEpiWarps);  // MMA done + every epilogue warp done with the weights
+      mbar_init(&sm.q_empty[i], 1 + kEpiWarps);    // MMA done + every epilogue warp holds its weights
       mbar_init(&sm.acc_full[i], 1);
       mbar_init(&sm.acc_empty[i], kEpiWarps);      // one arrive per epilogue warp
     }
@@ -226,7 +265,7 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
     for (int i = threadIdx.x; i <= A.batch; i += kThreads) sm.seq_meta[i] = __ldg(A.qsl + i);
     for (int i = threadIdx.x; i < A.batch; i += kThreads) sm.seq_meta[A.batch + 1 + i] = __ldg(A.seq_lens + i);
     __syncthreads();
-    if (warp == 0) build_item_table(A, sm.seq_meta, sm.item_off, sm.chunks);
+    if (warp == 0) build_item_table(A, sm);
   }
   if (warp == kMmaWarp) tmem_alloc(&sm.tmem_slot, 512);
   tc_fence_before();
@@ -235,82 +274,72 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
   const uint32_t tmem = sm.tmem_slot;
   volatile int* abort = &sm.abort;
   const int n_items = dense ? sm.item_off[A.batch] : A.n_chunks * A.batch * A.n_groups;
-  const auto item_at = [&](int item) {
-    return dense ? decode_dense(A, sm.seq_meta, sm.item_off, sm.chunks, item) : decode_item(A, sm.seq_meta, item);
-  };
+  const auto item_at = [&](int item) { return dense ? decode_dense(A, sm, item) : decode_sparse(A, item); };
 
-  if (warp >= kEpiWarps && warp < kMmaWarp) {
-    // ------------------------------ producers ------------------------------
-    // Lane l always copies 16-byte chunk (l % kCh) of rows l / kCh + i * kRowStep;
-    // a tile spans kTile / kBS blocks whose bases lanes 0.. load once per tile.
-    constexpr int kCh = kD / 16;
-    constexpr int kRowStep = 32 / kCh;
-    constexpr int kIters = kTile / kRowStep;
-    constexpr int kBlocks = kTile / kBS;
-    static_assert(kTile % kBS == 0 && kBS % kRowStep == 0 && kBlocks <= 32 && kBS % 4 == 0, "tile geometry");
-    const int pw = warp - kEpiWarps;
-    const int ch = lane % kCh, r0 = lane / kCh;
+  if (warp == kProducerWarp) {
+    // ------------------------------ producer (TMA) ------------------------------
     const int64_t layer_off = static_cast<int64_t>(A.layer) * A.L.layer_stride;
-    uint32_t k = 0, nitem = 0;
+    uint32_t k = 0, nitem = 0, nq = 0;  // key tiles, items, query loads issued
     for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
       const Item it = item_at(item);
       if (!it.valid) continue;
       const int32_t* bt = A.block_table + static_cast<int64_t>(it.b) * A.bt_stride;
-      if (pw == 0) {
+      {
         const int qb = nitem & 1;
         if (!mbar_wait(&sm.q_empty[qb], ((nitem >> 1) & 1) ^ 1, A.err, abort)) break;
-        const int rows = it.n_grp * H;
-        const uint32_t qbase = smem_u32(sm.q[qb]);
-        const uint8_t* qsrc = A.q_idx + static_cast<int64_t>(it.t0) * H * kD + ch * 16;
-        for (int r = r0; r < rows; r += kRowStep) cp_async16(qbase + sw128_off(r, ch), qsrc + r * kD, 16);
-        // the group's weights (n_grp * H floats, contiguous rows of w) ride along with q
-        const float* wsrc = A.w + static_cast<int64_t>(it.t0) * H;
-        for (int i = lane; i < rows / 4; i += 32) cp_async16(smem_u32(&sm.w[qb][i]), wsrc + 4 * i, 16);
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async();
+        if (lane == 0) {
+          const uint32_t wbytes = static_cast<uint32_t>(it.n_grp * H * 4);
+          mbar_arrive_expect_tx(&sm.q_full[qb], kGroup * H * kD + wbytes);
+          tma_load_2d(smem_u32(sm.q[qb]), &q_map, 0, it.t0 * H, &sm.q_full[qb]);
+          bulk_load(smem_u32(&sm.w[qb][0]), A.w + static_cast<int64_t>(it.t0) * H, wbytes, &sm.q_full[qb]);
+        }
+        ++nq;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.q_full[qb]);
       }
+      bool ok = true;
       for (int tile = 0; tile < it.n_tiles; ++tile, ++k) {
-        if (static_cast<int>(k % kProducers) != pw) continue;
         const int s = k % kStages;
         const int j0 = it.key_begin + tile * kTile;
-        unsigned long long kbase = 0;  // lane b < kBlocks: base of block b of the tile (0 = skip)
+        // lane b < kBlocks: physical block of the tile's b-th block; num_blocks loads zeros
+        int blk = static_cast<int>(A.L.num_blocks);
+        bool have = false;
         if (lane < kBlocks && j0 + lane * kBS < it.key_end) {
-          const int blk = __ldg(bt + (j0 + lane * kBS) / kBS);
-          if (blk < 0 || blk >= A.L.num_blocks) {
+          const int v = __ldg(bt + (j0 + lane * kBS) / kBS);
+          if (v < 0 || v >= A.L.num_blocks) {
             latch_error(A.err, SMLA_ERR_BAD_INDEX);
           } else {
-            kbase = reinterpret_cast<unsigned long long>(A.pool + static_cast<int64_t>(blk) * A.L.block_stride + layer_off);
+            blk = v;
+            have = true;
           }
         }
-        if (!mbar_wait(&sm.key_empty[s], ((k / kStages) & 1) ^ 1, A.err, abort)) break;
-        const uint32_t base = smem_u32(sm.keys[s]);
-#pragma unroll
-        for (int i = 0; i < kIters; ++i) {
-          const int r = r0 + i * kRowStep;
-          const unsigned long long b = __shfl_sync(0xffffffffu, kbase, (i * kRowStep) / kBS);
-          const bool ok = b != 0 && j0 + r < it.key_end;
-          const uint8_t* src = ok ? reinterpret_cast<const uint8_t*>(b) + A.L.idx_key_off + (r % kBS) * kD + ch * 16
-                                  : A.pool;
-          cp_async16(base + sw128_off(r, ch), src, ok ? 16u : 0u);
+        const uint32_t n_have = __popc(__ballot_sync(0xffffffffu, have));
+        if (!mbar_wait(&sm.key_empty[s], ((k / kStages) & 1) ^ 1, A.err, abort)) {
+          ok = false;
+          break;
         }
-        {
-          // key scales: lane l copies keys 4l..4l+3 (never straddling a block)
-          const unsigned long long b = __shfl_sync(0xffffffffu, kbase, (4 * lane) / kBS);
-          const bool ok = b != 0 && j0 + 4 * lane < it.key_end;
-          const uint8_t* src =
-              ok ? reinterpret_cast<const uint8_t*>(b) + A.L.idx_scale_off + ((4 * lane) % kBS) * 4 : A.pool;
-          cp_async16(smem_u32(&sm.kscale[s][4 * lane]), src, ok ? 16u : 0u);
-        }
-        cp_async_commit();
-        cp_async_wait<0>();
-        fence_proxy_async();
+        if (lane == 0) mbar_arrive_expect_tx(&sm.key_full[s], kTile * kD + n_have * kBS * 4);
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.key_full[s]);
+        if (lane < kBlocks) {
+          tma_load_3d(smem_u32(sm.keys[s]) + lane * kBS * kD, &key_map, 0, 0, blk, &sm.key_full[s]);
+          if (have)
+            bulk_load(smem_u32(&sm.kscale[s][lane * kBS]),
+                      A.pool + static_cast<int64_t>(blk) * A.L.block_stride + layer_off + A.L.idx_scale_off,
+                      kBS * 4, &sm.key_full[s]);
+        }
       }
+      if (!ok) break;
       ++nitem;
+    }
+    // Leave only after the copies issued last have landed (they have, unless a wait timed out).
+    if (lane == 0) {
+      for (uint32_t i = 0; i < kStages && i < k; ++i) {
+        const uint32_t kk = k - 1 - i;
+        mbar_drain(&sm.key_full[kk % kStages], (kk / kStages) & 1);
+      }
+      for (uint32_t i = 0; i < 2 && i < nq; ++i) {
+        const uint32_t qq = nq - 1 - i;
+        mbar_drain(&sm.q_full[qq & 1], (qq >> 1) & 1);
+      }
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
@@ -336,9 +365,9 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
           }
           tc_fence_after();
           const uint32_t kaddr = smem_u32(sm.keys[s]);
-          for (int kk = 0; kk < D / 32; ++kk) {
-            mma_f8(tmem + ab * 256, sw128_desc(kaddr + kk * 32, 16, 1024), sw128_desc(qaddr + kk * 32, 16, 1024),
-                   idesc, kk > 0);
+#pragma unroll
+          for (int kk = 0; kk < kD / 32; ++kk) {
+            mma_f8(tmem + ab * 256, key_desc<kD>(kaddr + kk * 32), key_desc<kD>(qaddr + kk * 32), idesc, kk > 0);
           }
           issued = true;
           mma_commit(&sm.key_empty[s]);
@@ -350,11 +379,12 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       }
       if (issued) {
         mma_commit(&sm.final_bar);
-        mbar_wait(&sm.final_bar, 0, A.err, abort);
+        mbar_drain(&sm.final_bar, 0);
       }
     }
   } else {
     // ------------------------------ epilogue (warps 0-15) ------------------------------
+    static_assert(kEpiWarps / 4 == kGroup, "one epilogue warp per query token of the group");
     const int row = (warp & 3) * 32 + lane;  // TMEM lane == key within the tile
     const int tok = warp >> 2;               // query token of the group handled by this warp
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -364,10 +394,29 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
       if (!it.valid) continue;
       const int qb = nitem & 1;
       if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
-      const float4* wq = sm.w[qb];
+      // this warp's token weights stay in registers for the whole item
+      float wr[H];
+      {
+        const float* wf = reinterpret_cast<const float*>(sm.w[qb]) + min(tok, it.n_grp - 1) * H;
+#pragma unroll
+        for (int x = 0; x < H; x += 4) {
+          const float4 v = *reinterpret_cast<const float4*>(wf + x);
+          wr[x] = v.x;
+          wr[x + 1] = v.y;
+          wr[x + 2] = v.z;
+          wr[x + 3] = v.w;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_relaxed(&sm.q_empty[qb]);  // the weights are in registers now
+      const bool mine = tok < it.n_grp;
+      // keys j < j_end of this token's row are stored (causal bound and chunk bound)
+      const int j_end = min(it.p_first + tok + 1, it.key_end);
+      float* srow = A.scores + static_cast<int64_t>(it.t0 + tok - A.tok_begin) * A.scores_stride;
+      const int n_tiles = it.n_tiles;
+      int j = it.key_begin + row;
       bool ok = true;
-      for (int tile = 0; tile < it.n_tiles; ++tile, ++a) {
-        const int j = it.key_begin + tile * kTile + row;
+      for (int tile = 0; tile < n_tiles; ++tile, ++a, j += kTile) {
         const int ab = a & 1;
         if (!mbar_wait(&sm.acc_full[ab], (a >> 1) & 1, A.err, abort)) {
           ok = false;
@@ -376,28 +425,24 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         tc_fence_after();
         const int st = a % kStages;  // the MMA consumed global tile a from stage a % kStages
         const float s_key = sm.kscale[st][row];
-        for (int i = tok; i < it.n_grp; i += kEpiWarps / 4) {
+        if (mine) {
           // two packed accumulator pairs: head h goes to lane h % 4 of (acc01, acc23)
           float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int h0 = 0; h0 < H; h0 += 32) {
-            uint32_t v[32];
-            tmem_ld32(tmem + lane_base + ab * 256 + i * H + h0, v);
+          for (int h0 = 0; h0 < H; h0 += 16) {
+            uint32_t v[16];
+            tmem_ld16(tmem + lane_base + ab * 256 + tok * H + h0, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int x = 0; x < 32 && h0 + x < H; x += 4) {
-              const float4 wv = wq[(i * H + h0 + x) / 4];
-              const float2 r01 = make_float2(fmaxf(__uint_as_float(v[x]), 0.f), fmaxf(__uint_as_float(v[x + 1]), 0.f));
-              const float2 r23 =
-                  make_float2(fmaxf(__uint_as_float(v[x + 2]), 0.f), fmaxf(__uint_as_float(v[x + 3]), 0.f));
-              acc01 = ffma2(r01, make_float2(wv.x, wv.y), acc01);
-              acc23 = ffma2(r23, make_float2(wv.z, wv.w), acc23);
+            for (int x = 0; x < 16 && h0 + x < H; x += 4) {
+              acc01 = ffma2(make_float2(fmaxf(__uint_as_float(v[x]), 0.f), fmaxf(__uint_as_float(v[x + 1]), 0.f)),
+                            make_float2(wr[h0 + x], wr[h0 + x + 1]), acc01);
+              acc23 = ffma2(make_float2(fmaxf(__uint_as_float(v[x + 2]), 0.f), fmaxf(__uint_as_float(v[x + 3]), 0.f)),
+                            make_float2(wr[h0 + x + 2], wr[h0 + x + 3]), acc23);
             }
           }
           const float total = (acc01.x + acc01.y) + (acc23.x + acc23.y);
-          if (j <= it.p_first + i && j < it.key_end) {
-            A.scores[static_cast<int64_t>(it.t0 + i - A.tok_begin) * A.scores_stride + j] = total * s_key;
-          }
+          if (j < j_end) srow[j] = total * s_key;
         }
         tc_fence_before();
         __syncwarp();
@@ -407,8 +452,6 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
         }
       }
       if (!ok) break;
-      __syncwarp();
-      if (lane == 0) mbar_arrive_relaxed(&sm.q_empty[qb]);  // this warp is done with the item's weights
       ++nitem;
     }
   }
@@ -421,8 +464,54 @@ __global__ void __launch_bounds__(kThreads, 1) index_scores_kernel(const IdxArgs
   }
 }
 
+// ---------------------------------------------------------------------------
+// Host side: tensor maps and launch
+// ---------------------------------------------------------------------------
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+  static EncodeTiledFn fn = nullptr;
+  if (fn == nullptr) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
 template <int kH, int kD, int kBS>
-smla_status_t launch_shape(const IdxArgs& A, int grid, cudaStream_t stream) {
+smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_rows, int grid, cudaStream_t stream) {
+  EncodeTiledFn enc = encode_tiled();
+  if (enc == nullptr) return SMLA_ERR_CUDA;
+  const CUtensorMapSwizzle swz = kD == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
+  CUtensorMap key_map, q_map;
+  {
+    // keys: [num_blocks][block_size][kD] bytes of one layer's indexer-key region
+    void* base = const_cast<uint8_t*>(A.pool) + static_cast<int64_t>(A.layer) * A.L.layer_stride + A.L.idx_key_off;
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kBS),
+                                static_cast<cuuint64_t>(A.L.num_blocks)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(A.L.block_stride)};
+    const cuuint32_t box[3] = {kD, kBS, 1};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (enc(&key_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SMLA_ERR_CUDA;
+  }
+  {
+    // query rows: [tokens * heads][kD] bytes; one box = the kGroup tokens of a work item
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(n_token_rows) * kH};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kD)};
+    const cuuint32_t box[2] = {kD, kGroup * kH};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(q_idx), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return SMLA_ERR_CUDA;
+  }
   const size_t smem = sizeof(IdxSmem) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -431,7 +520,7 @@ smla_status_t launch_shape(const IdxArgs& A, int grid, cudaStream_t stream) {
       return SMLA_ERR_CUDA;
     attr_set = true;
   }
-  index_scores_kernel<kH, kD, kBS><<<grid, kThreads, smem, stream>>>(A);
+  index_scores_kernel<kH, kD, kBS><<<grid, kThreads, smem, stream>>>(A, key_map, q_map);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
@@ -443,14 +532,11 @@ smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const 
                                   int tok_end, int max_q, int max_ctx, float* scores, int64_t scores_stride,
                                   cudaStream_t stream, unsigned* err) {
   if (tok_end <= tok_begin || max_ctx <= 0) return SMLA_OK;
-  if (n_idx_heads * kGroup > kMaxN || n_idx_heads > 64 || L.d_index % 32 != 0 || L.d_index > 128)
-    return SMLA_ERR_UNSUPPORTED;
   IdxArgs A;
   A.L = L;
   A.n_idx_heads = n_idx_heads;
   A.layer = layer;
   A.pool = static_cast<const uint8_t*>(pool);
-  A.q_idx = q_idx;
   A.w = w;
   A.block_table = block_table;
   A.bt_stride = bt_stride;
@@ -469,10 +555,15 @@ smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const 
   if (items <= 0) return SMLA_OK;
   const long long sms = device_sm_count();
   const int grid = static_cast<int>(items < sms ? items : sms);
+  // Query rows are addressed by absolute token (token t -> rows t*heads ..), so the map spans every
+  // token below tok_end; the box of a group near the end reads past it as zeros.
   // Shapes built into the library: (indexer heads, key dims, block size).
-  if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 64) return launch_shape<64, 128, 64>(A, grid, stream);
-  if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 16) return launch_shape<64, 128, 16>(A, grid, stream);
-  if (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16) return launch_shape<4, 32, 16>(A, grid, stream);
+  if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 64)
+    return launch_shape<64, 128, 64>(A, q_idx, tok_end, grid, stream);
+  if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 16)
+    return launch_shape<64, 128, 16>(A, q_idx, tok_end, grid, stream);
+  if (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16)
+    return launch_shape<4, 32, 16>(A, q_idx, tok_end, grid, stream);
   return SMLA_ERR_UNSUPPORTED;
 }
 
