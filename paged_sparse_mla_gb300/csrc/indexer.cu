@@ -43,7 +43,13 @@ constexpr int kChunkTiles = 16;    // tiles per work item (2048 keys)
 constexpr int kEpiWarps = 16;      // four warps per TMEM sub-partition, one query token each
 constexpr int kProducerWarp = kEpiWarps;
 constexpr int kMmaWarp = kEpiWarps + 1;
-constexpr int kThreads = 32 * (kEpiWarps + 2);
+constexpr int kThreads = 32 * (kEpiWarps + 4);  // warpgroup 4: producer, MMA issuer, two idle warps
+// Register split: the launch gives every thread kLaunchRegs (five warps per SM sub-partition);
+// setmaxnreg then moves registers from warpgroup 4 to the epilogue warpgroups.
+constexpr int kLaunchRegs = 96;
+constexpr int kEpiRegs = 104;
+constexpr int kOtherRegs = 56;
+static_assert(32 * kEpiWarps * kEpiRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr int kMaxN = 256;         // MMA N limit
 constexpr int kMaxSeqSmem = 1024;  // batches up to this size are scheduled densely
 
@@ -217,14 +223,29 @@ __device__ void build_item_table(const IdxArgs& A, IdxSmem& sm) {
   if (lane == 31) sm.item_off[A.batch] = incl;
 }
 
-__device__ __forceinline__ float2 ffma2(float2 a, float2 b, float2 c) {
-  unsigned long long d;
-  asm("{\n\t.reg .b64 ra, rb, rc;\n\t"
-      "mov.b64 ra, {%1, %2};\n\tmov.b64 rb, {%3, %4};\n\tmov.b64 rc, {%5, %6};\n\t"
-      "fma.rn.f32x2 %0, ra, rb, rc;\n\t}"
-      : "=l"(d)
-      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-  return make_float2(__uint_as_float(static_cast<uint32_t>(d)), __uint_as_float(static_cast<uint32_t>(d >> 32)));
+// Four heads of one key: acc0 += ReLU(v0, v1) * w01 and acc1 += (v2 + |v2|, v3 + |v3|) * w23,
+// with packed fp32 pairs.  The second pair carries twice the ReLU-weighted sum (exactly: a
+// factor of two commutes with rounding), which moves half of the ReLUs from the integer/
+// compare pipe onto the FMA pipe; the caller halves acc1's total.
+__device__ __forceinline__ void relu_fma4(uint64_t& acc0, uint64_t& acc1, uint32_t v0, uint32_t v1, uint32_t v2,
+                                          uint32_t v3, uint64_t w01, uint64_t w23) {
+  asm("{\n\t.reg .f32 a0, a1, b0, b1;\n\t.reg .b64 p, q;\n\t"
+      "max.f32 a0, %2, 0f00000000;\n\t"
+      "max.f32 a1, %3, 0f00000000;\n\t"
+      "abs.f32 b0, %4;\n\t"
+      "abs.f32 b1, %5;\n\t"
+      "add.rn.f32 b0, b0, %4;\n\t"
+      "add.rn.f32 b1, b1, %5;\n\t"
+      "mov.b64 p, {a0, a1};\n\t"
+      "mov.b64 q, {b0, b1};\n\t"
+      "fma.rn.f32x2 %0, p, %6, %0;\n\t"
+      "fma.rn.f32x2 %1, q, %7, %1;\n\t}"
+      : "+l"(acc0), "+l"(acc1)
+      : "r"(v0), "r"(v1), "r"(v2), "r"(v3), "l"(w01), "l"(w23));
+}
+
+__device__ __forceinline__ float pair_sum(uint64_t p) {
+  return __uint_as_float(static_cast<uint32_t>(p)) + __uint_as_float(static_cast<uint32_t>(p >> 32));
 }
 
 __device__ __forceinline__ int mma_n(int n_grp, int heads) {
@@ -278,33 +299,62 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == kProducerWarp) {
     // ------------------------------ producer (TMA) ------------------------------
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     const int64_t layer_off = static_cast<int64_t>(A.layer) * A.L.layer_stride;
-    uint32_t k = 0, nitem = 0, nq = 0;  // key tiles, items, query loads issued
-    for (int item = blockIdx.x; item < n_items && !*abort; item += gridDim.x) {
-      const Item it = item_at(item);
-      if (!it.valid) continue;
+    // Block-table entries of a whole item (kItemBlocks blocks) are fetched one item ahead:
+    // lane l holds the entries of the item's blocks l, l + 32, ... (blocks past the item's
+    // last key are not read).  Each tile then takes its kBlocks entries from the owning lanes.
+    constexpr int kItemBlocks = kChunkTiles * kBlocks;
+    constexpr int kPer = (kItemBlocks + 31) / 32;
+    static_assert(32 % kBlocks == 0, "a tile's block entries sit in one register slot");
+    const auto fetch_bt = [&](const Item& it, int (&dst)[kPer]) {
       const int32_t* bt = A.block_table + static_cast<int64_t>(it.b) * A.bt_stride;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) {
+        const int key0 = it.key_begin + (lane + 32 * i) * kBS;
+        dst[i] = key0 < it.key_end ? __ldg(bt + key0 / kBS) : -1;
+      }
+    };
+    const auto next_valid = [&](int item, Item& it) {
+      for (; item < n_items; item += gridDim.x) {
+        it = item_at(item);
+        if (it.valid) return item;
+      }
+      return n_items;
+    };
+    uint32_t k = 0, nq = 0;  // key tiles and query loads issued
+    Item cur, nxt;
+    int bt_cur[kPer], bt_nxt[kPer];
+    int item = next_valid(blockIdx.x, cur);
+    if (item < n_items) fetch_bt(cur, bt_cur);
+    while (item < n_items && !*abort) {
+      const int item_n = next_valid(item + gridDim.x, nxt);
+      if (item_n < n_items) fetch_bt(nxt, bt_nxt);  // in flight while this item's tiles are issued
       {
-        const int qb = nitem & 1;
-        if (!mbar_wait(&sm.q_empty[qb], ((nitem >> 1) & 1) ^ 1, A.err, abort)) break;
+        const int qb = nq & 1;
+        if (!mbar_wait(&sm.q_empty[qb], ((nq >> 1) & 1) ^ 1, A.err, abort)) break;
         if (lane == 0) {
-          const uint32_t wbytes = static_cast<uint32_t>(it.n_grp * H * 4);
+          const uint32_t wbytes = static_cast<uint32_t>(cur.n_grp * H * 4);
           mbar_arrive_expect_tx(&sm.q_full[qb], kGroup * H * kD + wbytes);
-          tma_load_2d(smem_u32(sm.q[qb]), &q_map, 0, it.t0 * H, &sm.q_full[qb]);
-          bulk_load(smem_u32(&sm.w[qb][0]), A.w + static_cast<int64_t>(it.t0) * H, wbytes, &sm.q_full[qb]);
+          tma_load_2d(smem_u32(sm.q[qb]), &q_map, 0, cur.t0 * H, &sm.q_full[qb]);
+          bulk_load(smem_u32(&sm.w[qb][0]), A.w + static_cast<int64_t>(cur.t0) * H, wbytes, &sm.q_full[qb]);
         }
         ++nq;
         __syncwarp();
       }
       bool ok = true;
-      for (int tile = 0; tile < it.n_tiles; ++tile, ++k) {
+      for (int tile = 0; tile < cur.n_tiles; ++tile, ++k) {
         const int s = k % kStages;
-        const int j0 = it.key_begin + tile * kTile;
         // lane b < kBlocks: physical block of the tile's b-th block; num_blocks loads zeros
+        const int e = tile * kBlocks + (lane % kBlocks);
+        const int slot = (tile * kBlocks) / 32;
+        int mine_v = bt_cur[0];
+#pragma unroll
+        for (int i = 1; i < kPer; ++i) mine_v = slot == i ? bt_cur[i] : mine_v;
+        const int v = __shfl_sync(0xffffffffu, mine_v, e % 32);
         int blk = static_cast<int>(A.L.num_blocks);
         bool have = false;
-        if (lane < kBlocks && j0 + lane * kBS < it.key_end) {
-          const int v = __ldg(bt + (j0 + lane * kBS) / kBS);
+        if (lane < kBlocks && cur.key_begin + tile * kTile + lane * kBS < cur.key_end) {
           if (v < 0 || v >= A.L.num_blocks) {
             latch_error(A.err, SMLA_ERR_BAD_INDEX);
           } else {
@@ -328,7 +378,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       if (!ok) break;
-      ++nitem;
+      item = item_n;
+      cur = nxt;
+#pragma unroll
+      for (int i = 0; i < kPer; ++i) bt_cur[i] = bt_nxt[i];
     }
     // Leave only after the copies issued last have landed (they have, unless a wait timed out).
     if (lane == 0) {
@@ -343,6 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     if (lane == 0) {
       uint32_t k = 0, nitem = 0, a = 0;
       bool issued = false;
@@ -382,8 +436,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_drain(&sm.final_bar, 0);
       }
     }
+  } else if (warp >= kEpiWarps) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));  // idle
   } else {
     // ------------------------------ epilogue (warps 0-15) ------------------------------
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kEpiRegs));
     static_assert(kEpiWarps / 4 == kGroup, "one epilogue warp per query token of the group");
     const int row = (warp & 3) * 32 + lane;  // TMEM lane == key within the tile
     const int tok = warp >> 2;               // query token of the group handled by this warp
@@ -394,17 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!it.valid) continue;
       const int qb = nitem & 1;
       if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
-      // this warp's token weights stay in registers for the whole item
-      float wr[H];
+      // this warp's token weights stay in registers for the whole item, as packed pairs
+      uint64_t wp[H / 2];
       {
         const float* wf = reinterpret_cast<const float*>(sm.w[qb]) + min(tok, it.n_grp - 1) * H;
 #pragma unroll
         for (int x = 0; x < H; x += 4) {
-          const float4 v = *reinterpret_cast<const float4*>(wf + x);
-          wr[x] = v.x;
-          wr[x + 1] = v.y;
-          wr[x + 2] = v.z;
-          wr[x + 3] = v.w;
+          const ulonglong2 v = *reinterpret_cast<const ulonglong2*>(wf + x);
+          wp[x / 2] = v.x;
+          wp[x / 2 + 1] = v.y;
         }
       }
       __syncwarp();
@@ -426,22 +481,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = a % kStages;  // the MMA consumed global tile a from stage a % kStages
         const float s_key = sm.kscale[st][row];
         if (mine) {
-          // two packed accumulator pairs: head h goes to lane h % 4 of (acc01, acc23)
-          float2 acc01 = make_float2(0.f, 0.f), acc23 = make_float2(0.f, 0.f);
+          // head h goes to element h % 2 of acc0 (h % 4 < 2) or of acc1 (h % 4 >= 2, doubled)
+          // 16-column TMEM loads, the next one in flight while the current one is reduced
+          uint64_t acc0 = 0, acc1 = 0;
+          const uint32_t tbase = tmem + lane_base + ab * 256 + tok * H;
+          uint32_t v[2][16];
+          tmem_ld16(tbase, v[0]);
+          tmem_ld_wait(v[0]);
 #pragma unroll
-          for (int h0 = 0; h0 < H; h0 += 16) {
-            uint32_t v[16];
-            tmem_ld16(tmem + lane_base + ab * 256 + tok * H + h0, v);
-            tmem_ld_wait();
+          for (int c = 0; c < (H + 15) / 16; ++c) {
+            const bool more = (c + 1) * 16 < H;
+            if (more) tmem_ld16(tbase + (c + 1) * 16, v[(c + 1) & 1]);
 #pragma unroll
-            for (int x = 0; x < 16 && h0 + x < H; x += 4) {
-              acc01 = ffma2(make_float2(fmaxf(__uint_as_float(v[x]), 0.f), fmaxf(__uint_as_float(v[x + 1]), 0.f)),
-                            make_float2(wr[h0 + x], wr[h0 + x + 1]), acc01);
-              acc23 = ffma2(make_float2(fmaxf(__uint_as_float(v[x + 2]), 0.f), fmaxf(__uint_as_float(v[x + 3]), 0.f)),
-                            make_float2(wr[h0 + x + 2], wr[h0 + x + 3]), acc23);
-            }
+            for (int x = 0; x < 16 && c * 16 + x < H; x += 4)
+              relu_fma4(acc0, acc1, v[c & 1][x], v[c & 1][x + 1], v[c & 1][x + 2], v[c & 1][x + 3],
+                        wp[(c * 16 + x) / 2], wp[(c * 16 + x) / 2 + 1]);
+            if (more) tmem_ld_wait(v[(c + 1) & 1]);
           }
-          const float total = (acc01.x + acc01.y) + (acc23.x + acc23.y);
+          const float total = pair_sum(acc0) + 0.5f * pair_sum(acc1);
           if (j < j_end) srow[j] = total * s_key;
         }
         tc_fence_before();
@@ -518,6 +575,11 @@ smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_r
     if (cudaFuncSetAttribute(index_scores_kernel<kH, kD, kBS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
+    // setmaxnreg.inc can only draw on the registers the CTA was launched with;
+    // refuse to launch if the compiled allocation does not cover the split.
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, index_scores_kernel<kH, kD, kBS>) != cudaSuccess) return SMLA_ERR_CUDA;
+    if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set = true;
   }
   index_scores_kernel<kH, kD, kBS><<<grid, kThreads, smem, stream>>>(A, key_map, q_map);
