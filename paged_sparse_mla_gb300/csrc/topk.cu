@@ -324,12 +324,14 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
                                     &sm.n_cand, kCap);
   };
   if ((reinterpret_cast<uintptr_t>(s) & 15) == 0) {
+    // Each iteration a thread holds U float4 (16 keys); the next iteration's loads are issued
+    // before this one is filtered.  A warp reserves room for all its hits with one atomic.
     constexpr int U = 4;
+    const int lane = threadIdx.x & 31;
     const int n4 = (n + 3) / 4;
     const int span = kThreads * U;
     const int bound = (n4 + span - 1) / span * span;
-    for (int base = threadIdx.x; base < bound; base += span) {
-      float4 v[U];
+    const auto load = [&](int base, float4 (&v)[U]) {
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = 4 * (base + u * kThreads);
@@ -342,18 +344,51 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
           if (j + 2 < n) v[u].z = __ldg(s + j + 2);
         }
       }
+    };
+    float4 cur[U], nxt[U];
+    load(threadIdx.x, cur);
+    for (int base = threadIdx.x; base < bound; base += span) {
+      if (base + span < bound) load(base + span, nxt);
+      uint32_t keys[4 * U];
+      uint32_t hit = 0;
 #pragma unroll
       for (int u = 0; u < U; ++u) {
         const int j = 4 * (base + u * kThreads);
-        const bool hit = (j < n && order_key(v[u].x) >= thr) || (j + 1 < n && order_key(v[u].y) >= thr) ||
-                         (j + 2 < n && order_key(v[u].z) >= thr) || (j + 3 < n && order_key(v[u].w) >= thr);
-        if (__any_sync(0xffffffffu, hit)) {
-          collect(j, v[u].x, j < n);
-          collect(j + 1, v[u].y, j + 1 < n);
-          collect(j + 2, v[u].z, j + 2 < n);
-          collect(j + 3, v[u].w, j + 3 < n);
+        keys[4 * u] = order_key(cur[u].x);
+        keys[4 * u + 1] = order_key(cur[u].y);
+        keys[4 * u + 2] = order_key(cur[u].z);
+        keys[4 * u + 3] = order_key(cur[u].w);
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+          if (j + e < n && keys[4 * u + e] >= thr) hit |= 1u << (4 * u + e);
+      }
+      const int cnt = __popc(hit);
+      int incl = cnt;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += y;
+      }
+      const int total = __shfl_sync(0xffffffffu, incl, 31);
+      if (total > 0) {
+        int pos = 0;
+        if (lane == 31) pos = atomicAdd(&sm.n_cand, total);
+        pos = __shfl_sync(0xffffffffu, pos, 31) + incl - cnt;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            if (hit & (1u << (4 * u + e))) {
+              const int j = 4 * (base + u * kThreads) + e;
+              if (pos < kCap)
+                sm.cand[pos] = (static_cast<unsigned long long>(keys[4 * u + e]) << 32) | static_cast<uint32_t>(~j);
+              ++pos;
+            }
+          }
         }
       }
+#pragma unroll
+      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
     }
   } else {
     for_row(s, n, collect);
