@@ -7,22 +7,28 @@
 // log-sum-exp statistics so partial results can be merged.
 //
 // Design (sm_103a, one persistent CTA per SM, one query token at a time):
-//   * 128 selected positions form a tile.  Eleven producer warps translate the
-//     logical positions through the block table, read the 656-byte records
-//     (L2 prefetch of the next tile with cp.async.bulk.prefetch), dequantise the
-//     E4M3 latent with its per-128 fp32 scales to bf16, and write the tile as
-//     9 chunks of [128 keys x 64 dims] with the 128-byte swizzle (8 latent
-//     chunks + 1 rope chunk); the query is staged the same way (64 heads).
-//   * MMA1 (warp 12): S^T[key, head] = Khat[key, :] . q[head, :] over 576 dims,
-//     M = 128 keys, N = 64 heads, fp32 in tensor memory.  TMEM lane = key.
-//   * Softmax (warps 0-3, thread = key): per-head tile maxima with a butterfly
+//   * 64 selected positions form a tile, and the tile buffer is double-buffered
+//     so that gathering tile t+1 overlaps the MMAs and the softmax of tile t.
+//     Eleven producer warps translate the logical positions through the block
+//     table two tiles ahead, read the 656-byte records (L2 prefetch with
+//     cp.async.bulk.prefetch), dequantise the E4M3 latent with its per-128 fp32
+//     scales to bf16, and write the tile as 9 chunks of [64 keys x 64 dims] with
+//     the 128-byte swizzle (8 latent chunks + 1 rope chunk); the query is staged
+//     the same way (64 heads).
+//   * MMA1 (warp 8): S^T[key, head] = Khat[key, :] . q[head, :] over 576 dims,
+//     M = 64 keys, N = 64 heads, fp32 in tensor memory, two buffers.  Key i of
+//     the tile sits in TMEM lane (i % 16) + 32 (i / 16).
+//   * Softmax (warps 0-7; warp w holds keys 16 (w % 4) .. + 15 and heads
+//     32 (w / 4) .. + 31): per-head tile maxima with a butterfly
 //     transpose-reduction across lanes, online softmax with lazy rescaling
 //     (the running max only moves when a head's tile max exceeds it by 2^8),
 //     P^T[key, head] written as bf16 into the rope chunk (free after MMA1),
 //     per-thread partial row sums.
 //   * MMA2: O^T[dim, head] += V^T[dim, key] . P^T[key, head] with both operands
 //     MN-major: the same swizzled latent chunks serve as V^T without a
-//     transpose; M = 128 dims x 4 tiles, N = 64 heads, K = 128 keys.
+//     transpose; M = 128 dims x 4 tiles, N = 64 heads, K = 64 keys.  The MMA
+//     warp issues MMA2 of tile t-1 as soon as its probabilities are ready (it
+//     releases that buffer to the producers), then MMA1 of tile t once gathered.
 //   * Epilogue: O^T / l -> bf16 out[t, h, d] (thread = dim, coalesced) and
 //     lse = ln(sum) from the running max and the reduced row sums.
 #include "smla_internal.h"
@@ -30,26 +36,29 @@
 namespace smla {
 namespace {
 
-constexpr int kTile = 128;     // keys per tile
+constexpr int kTile = 64;      // keys per tile (MMA1 M)
 constexpr int kHeads = 64;     // MMA N: query heads (zero padded)
-// Warp roles: warpgroup 0 = softmax (warps 0-3); warps 4-11 and 13-15 = producers;
-// warp 12 = MMA issuer.  setmaxnreg moves registers to the softmax warpgroup.
+// Warp roles: warpgroups 0-1 = softmax (warps 0-7); warp 8 = MMA issuer; warps 9-19 =
+// producers.  setmaxnreg moves registers to the softmax warpgroups.
+constexpr int kSoftmaxThreads = 256;
+constexpr int kMmaWarp = 8;
+constexpr int kFirstProducerWarp = 9;
 constexpr int kProducerThreads = 32 * 11;
-constexpr int kMmaWarp = 12;
-constexpr int kThreads = 32 * 16;
-constexpr int kLaunchRegs = 128;       // per thread at launch (65536 / 512)
-constexpr int kSoftmaxRegs = 216;
-constexpr int kOtherRegs = 96;         // 128*216 + 384*96 = 64512 <= 512*128
-static_assert(128 * kSoftmaxRegs + 384 * kOtherRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
+constexpr int kThreads = 32 * 20;
+constexpr int kLaunchRegs = 96;        // per thread at launch (65536 / 640, rounded down to 8)
+constexpr int kSoftmaxRegs = 120;
+constexpr int kOtherRegs = 80;         // 256*120 + 384*80 <= 640*96
+static_assert(kSoftmaxThreads * kSoftmaxRegs + (kThreads - kSoftmaxThreads) * kOtherRegs <= kThreads * kLaunchRegs,
+              "register split exceeds the launch");
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLn2 = 0.6931471805599453f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 template <int NCH>
 struct __align__(1024) AttnSmem {
-  uint8_t kv[NCH][kTile * 128];    // chunk c: [128 keys][64 dims] bf16, swizzled; chunk NCH-1: rope, then P^T
-  uint8_t q[NCH][kHeads * 128];    // chunk c: [64 heads][64 dims] bf16, swizzled
-  const uint8_t* rec[2][kTile];    // record address per key, current and next tile (nullptr = masked)
+  uint8_t kv[2][NCH][kTile * 128];  // buffer, chunk c: [64 keys][64 dims] bf16, swizzled; chunk NCH-1: rope, then P^T
+  uint8_t q[NCH][kHeads * 128];     // chunk c: [64 heads][64 dims] bf16, swizzled
+  const uint8_t* rec[3][kTile];     // record address per key of tiles t, t+1, t+2 (nullptr = masked)
   float red[4][kHeads];
   float m_tile[kHeads];
   float m_run[kHeads];
@@ -57,7 +66,9 @@ struct __align__(1024) AttnSmem {
   float l_fin[kHeads];
   int ntiles[2];
   uint64_t tok_full[2], tok_empty[2];
-  uint64_t q_full, q_empty, kv_full, kv_empty, s_full, p_full, o_done, final_bar;
+  uint64_t q_full, q_empty;
+  uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2];
+  uint64_t o_done, final_bar;
   uint32_t tmem_slot;
   int abort;
 };
@@ -79,14 +90,14 @@ struct AttnArgs {
   unsigned* err;
 };
 
-// Transpose-reduce 64 per-lane values across the 32 lanes of a warp: afterwards
-// lane l holds the reduction of heads 2l and 2l+1 in v[0], v[1].
+// Transpose-reduce 32 per-lane values across the 32 lanes of a warp: afterwards
+// lane l holds the reduction of value l in v[0].
 template <bool kMax>
-__device__ __forceinline__ void warp_transpose_reduce(float (&v)[kHeads], int lane) {
+__device__ __forceinline__ void warp_transpose_reduce32(float (&v)[32], int lane) {
 #pragma unroll
   for (int st = 0; st < 5; ++st) {
     const int off = 16 >> st;
-    const int half = 32 >> st;
+    const int half = 16 >> st;
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int i = 0; i < half; ++i) {
@@ -96,6 +107,13 @@ __device__ __forceinline__ void warp_transpose_reduce(float (&v)[kHeads], int la
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
+}
+
+// Maximum of v over the 32 lanes (every lane receives it).
+__device__ __forceinline__ float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
 }
 
 // 2^x with the hardware approximation (MUFU; relative error ~2^-22, -inf -> 0).
@@ -149,7 +167,7 @@ __device__ __forceinline__ void rope_unit(int ur, int& key, int& v) {
 // Loads for one batch of the producer unit stream (see the key-tile loop):
 // latent units fetch 16 E4M3 codes and their fp32 scale, rope units fetch 8
 // bf16 (zero padded past d_rope).  Masked keys (nullptr record) read as zero.
-constexpr int kBatch = 6;
+constexpr int kBatch = 4;
 __device__ __forceinline__ void load_units(const uint8_t* const* rec, int u0, int n_lat, int n_units, int parts,
                                            int DL, int DR, int qtile, int n_scales, bool rope16,
                                            uint4 (&val)[kBatch], float (&sc)[kBatch]) {
@@ -221,29 +239,32 @@ __device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
   return (last + kTile) / kTile;
 }
 
-template <int NCH>
+template <int NCH, bool WR>
 __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem<NCH>& sm =
       *reinterpret_cast<AttnSmem<NCH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kLatChunks = NCH - 1;
+  constexpr int kChunkBytes = kTile * 128;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   const KernelLayout& L = A.L;
   constexpr int DL = (NCH - 1) * 64;  // latent dims (8 chunks of 64 for 512)
+  constexpr int kDTiles = (DL + 127) / 128;
   const int DR = L.d_rope;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
       mbar_init(&sm.tok_full[i], 1);
-      mbar_init(&sm.tok_empty[i], 5);
+      mbar_init(&sm.tok_empty[i], 1 + kSoftmaxThreads / 32);
+      mbar_init(&sm.kv_full[i], kProducerThreads / 32);  // one arrive per producer warp
+      mbar_init(&sm.kv_empty[i], 1);                     // MMA2 of the tile done
+      mbar_init(&sm.s_full[i], 1);                       // MMA1 of the tile done
+      mbar_init(&sm.s_empty[i], kSoftmaxThreads / 32);   // scores read by every softmax warp
+      mbar_init(&sm.p_full[i], kSoftmaxThreads / 32);    // P^T written by every softmax warp
     }
-    mbar_init(&sm.q_full, kProducerThreads / 32);   // one arrive per producer warp
+    mbar_init(&sm.q_full, kProducerThreads / 32);
     mbar_init(&sm.q_empty, 1);
-    mbar_init(&sm.kv_full, kProducerThreads / 32);
-    mbar_init(&sm.kv_empty, 1);
-    mbar_init(&sm.s_full, 1);
-    mbar_init(&sm.p_full, 4);                        // one arrive per softmax warp
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.final_bar, 1);
     sm.abort = 0;
@@ -255,21 +276,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
   tc_fence_after();
   const uint32_t tmem = sm.tmem_slot;
   const uint32_t tmem_o = tmem;         // O^T: 4 d-tiles x 64 columns
-  const uint32_t tmem_s = tmem + 256;   // S^T: 64 columns
+  const uint32_t tmem_s = tmem + 256;   // S^T: two buffers of 64 columns
   volatile int* abort = &sm.abort;
 
-  if (warp >= 4 && warp != kMmaWarp) {
+  if (warp >= kFirstProducerWarp) {
     // ------------------------------ producers ------------------------------
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
-    const int ptid = threadIdx.x - 128 - (warp > kMmaWarp ? 32 : 0);  // 0..351
+    const int ptid = threadIdx.x - 32 * kFirstProducerWarp;  // 0..351
     uint32_t n = 0, nw = 0, kk = 0;
     constexpr int parts = DL / 16;       // 16-code parts per record
     const bool rope16 = ((DL + 4 * L.n_scales) % 16) == 0;
+    // WR: 512 latent codes, four per-128 scales and 64 rope values = 41 aligned 16-byte pieces
+    constexpr bool whole_records = WR;
     for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
       const int t = A.tok_begin + tr;
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
       const int ntiles = row_tiles(idx, A.top_k, lane);
-      if (warp == 4 && lane == 0) {
+      if (warp == kFirstProducerWarp && lane == 0) {
         if (!mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) break;
         sm.ntiles[n & 1] = ntiles;
         mbar_arrive(&sm.tok_full[n & 1]);
@@ -298,39 +321,105 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.q_full);
       // ---- key tiles ----
-      // Unit stream of one tile: units [0, 128*parts) are 16-code latent pieces,
-      // units [128*parts, 128*(parts+8)) are 16-byte rope pieces (see latent_unit).
+      // Unit stream of one tile: units [0, 64*parts) are 16-code latent pieces,
+      // units [64*parts, 64*(parts+8)) are 16-byte rope pieces (see latent_unit).
       constexpr int n_lat = kTile * parts;
       constexpr int n_units = n_lat + kTile * 8;
-      auto fill_rec = [&](int tile, int buf) {
-        for (int rr = ptid; rr < kTile; rr += kProducerThreads) {
-          const int e = tile * kTile + rr;
-          const int j = e < A.top_k ? __ldg(idx + e) : -1;
-          const uint8_t* r = nullptr;
-          if (j >= 0) {
-            const int blk = __ldg(bt + j / L.block_size);
-            if (blk < 0 || blk >= L.num_blocks) {
-              latch_error(A.err, SMLA_ERR_BAD_INDEX);
-            } else {
-              r = A.pool + static_cast<int64_t>(blk) * L.block_stride + static_cast<int64_t>(A.layer) * L.layer_stride +
-                  L.rec_off + static_cast<int64_t>(j % L.block_size) * L.rec_stride;
-              prefetch_l2_bulk(r, static_cast<uint32_t>(L.rec_stride));
-            }
-          }
-          sm.rec[buf][rr] = r;
+      // Record addresses run two tiles ahead of the gather: during tile t, thread p < 64 reads
+      // the top-k entry of key p of tile t+2 (before the gather), its block-table entry (after
+      // the first batch), and publishes the record address with an L2 prefetch (at the end).
+      const auto rec_of = [&](int j, int blk) -> const uint8_t* {
+        if (j < 0) return nullptr;
+        if (blk < 0 || blk >= L.num_blocks) {
+          latch_error(A.err, SMLA_ERR_BAD_INDEX);
+          return nullptr;
         }
+        const uint8_t* r = A.pool + static_cast<int64_t>(blk) * L.block_stride +
+                           static_cast<int64_t>(A.layer) * L.layer_stride + L.rec_off +
+                           static_cast<int64_t>(j % L.block_size) * L.rec_stride;
+        prefetch_l2_bulk(r, static_cast<uint32_t>(L.rec_stride));
+        return r;
       };
-      fill_rec(0, 0);
+      const auto entry = [&](int tile) -> int {
+        const int e = tile * kTile + ptid;
+        return (ptid < kTile && tile < ntiles && e < A.top_k) ? __ldg(idx + e) : -1;
+      };
+      const auto block_of = [&](int j) -> int { return j >= 0 ? __ldg(bt + j / L.block_size) : -1; };
+      if (ptid < kTile) {
+        const int j0 = entry(0), j1 = entry(1);
+        const int b0 = block_of(j0), b1 = block_of(j1);
+        sm.rec[0][ptid] = rec_of(j0, b0);
+        sm.rec[1][ptid] = rec_of(j1, b1);
+      }
       named_bar_sync(2, kProducerThreads);
       bool ok = true;
       for (int tile = 0; tile < ntiles; ++tile, ++kk) {
-        const uint8_t* const* rec = sm.rec[tile & 1];
+        const int kb = kk & 1;
+        const uint8_t* const* rec = sm.rec[tile % 3];
+        const int j_ahead = entry(tile + 2);
+        int blk_ahead = -1;
+        if constexpr (whole_records) {
+          // Whole-record gather: producer warp pw takes keys pw, pw + 11, ...; for each key,
+          // lane l loads latent piece l (16 codes) and, for l < 9, the piece after the latent
+          // codes (lane 0: the four scales; lanes 1-8: the rope), so every record is read by
+          // two coalesced warp loads.  Two keys per batch, three batches per tile.
+          const int pw = warp - kFirstProducerWarp;
+          constexpr int kPW = kProducerThreads / 32;
+          constexpr int kR = 2;
+          uint4 lat[2][kR], ext[2][kR];
+          const auto load_batch = [&](int i0, uint4 (&la)[kR], uint4 (&ex)[kR]) {
+#pragma unroll
+            for (int i = 0; i < kR; ++i) {
+              const int key = pw + kPW * (i0 + i);
+              const uint8_t* r = key < kTile ? rec[key] : nullptr;
+              la[i] = make_uint4(0, 0, 0, 0);
+              ex[i] = make_uint4(0, 0, 0, 0);
+              if (r != nullptr) {
+                la[i] = __ldg(reinterpret_cast<const uint4*>(r) + lane);
+                if (lane < 9) ex[i] = __ldg(reinterpret_cast<const uint4*>(r + DL) + lane);
+              }
+            }
+          };
+          const auto store_batch = [&](int i0, const uint4 (&la)[kR], const uint4 (&ex)[kR]) {
+#pragma unroll
+            for (int i = 0; i < kR; ++i) {
+              const int key = pw + kPW * (i0 + i);
+              if (key >= kTile) break;
+              const float s0 = __shfl_sync(0xffffffffu, __uint_as_float(ex[i].x), 0);
+              const float s1 = __shfl_sync(0xffffffffu, __uint_as_float(ex[i].y), 0);
+              const float s2 = __shfl_sync(0xffffffffu, __uint_as_float(ex[i].z), 0);
+              const float s3 = __shfl_sync(0xffffffffu, __uint_as_float(ex[i].w), 0);
+              const int qb = lane >> 3;  // 128-dim scale block of this lane's codes
+              const float sc = qb == 0 ? s0 : qb == 1 ? s1 : qb == 2 ? s2 : s3;
+              uint4 o0, o1;
+              dequant16(la[i], sc, o0, o1);
+              // chunk c = lane / 4, 16-byte slots 2 (lane % 4) and + 1; odd chunks store the
+              // second slot first so that a quarter-warp's stores hit eight different banks
+              const int c = lane >> 2, v0 = 2 * (lane & 3), odd = c & 1;
+              *reinterpret_cast<uint4*>(&sm.kv[kb][c][sw128_off(key, v0 + odd)]) = odd ? o1 : o0;
+              *reinterpret_cast<uint4*>(&sm.kv[kb][c][sw128_off(key, v0 + 1 - odd)]) = odd ? o0 : o1;
+              if (lane >= 1 && lane <= 8)
+                *reinterpret_cast<uint4*>(&sm.kv[kb][kLatChunks][sw128_off(key, lane - 1)]) = ex[i];
+            }
+          };
+          constexpr int kNB = ((kTile + kPW - 1) / kPW + kR - 1) / kR;  // batches per tile
+          load_batch(0, lat[0], ext[0]);
+          if (!mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort)) {
+            ok = false;
+            break;
+          }
+#pragma unroll
+          for (int bi = 0; bi < kNB; ++bi) {
+            if (bi + 1 < kNB) load_batch((bi + 1) * kR, lat[(bi + 1) & 1], ext[(bi + 1) & 1]);
+            if (bi == 0) blk_ahead = block_of(j_ahead);
+            store_batch(bi * kR, lat[bi & 1], ext[bi & 1]);
+          }
+        } else {
         // first batch of loads is issued before waiting for the tile buffer
         uint4 cur[kBatch];
         float csc[kBatch];
         load_units(rec, ptid, n_lat, n_units, parts, DL, DR, L.quant_tile, L.n_scales, rope16, cur, csc);
-        if (tile + 1 < ntiles) fill_rec(tile + 1, (tile + 1) & 1);  // addresses (and L2 warm-up) one tile ahead
-        if (!mbar_wait(&sm.kv_empty, (kk & 1) ^ 1, A.err, abort)) {
+        if (!mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort)) {
           ok = false;
           break;
         }
@@ -340,35 +429,38 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           const int nbase = base + kBatch * kProducerThreads;
           if (nbase < n_units)
             load_units(rec, nbase + ptid, n_lat, n_units, parts, DL, DR, L.quant_tile, L.n_scales, rope16, nxt, nsc);
+          if (base == 0) blk_ahead = block_of(j_ahead);
 #pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            const int u = base + ptid + b * kProducerThreads;
+          for (int bb = 0; bb < kBatch; ++bb) {
+            const int u = base + ptid + bb * kProducerThreads;
             if (u >= n_units) break;
             if (u < n_lat) {
               int r, part;
               latent_unit(u, parts, r, part);
               uint4 o0, o1;
-              dequant16(cur[b], csc[b], o0, o1);
+              dequant16(cur[bb], csc[bb], o0, o1);
               const int d0 = part * 16;
               const int c = d0 / 64, v0 = (d0 % 64) / 8;
-              *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0)]) = o0;
-              *reinterpret_cast<uint4*>(&sm.kv[c][sw128_off(r, v0 + 1)]) = o1;
+              *reinterpret_cast<uint4*>(&sm.kv[kb][c][sw128_off(r, v0)]) = o0;
+              *reinterpret_cast<uint4*>(&sm.kv[kb][c][sw128_off(r, v0 + 1)]) = o1;
             } else {
               int r, v;
               rope_unit(u - n_lat, r, v);
-              *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(r, v)]) = cur[b];
+              *reinterpret_cast<uint4*>(&sm.kv[kb][kLatChunks][sw128_off(r, v)]) = cur[bb];
             }
           }
 #pragma unroll
-          for (int b = 0; b < kBatch; ++b) {
-            cur[b] = nxt[b];
-            csc[b] = nsc[b];
+          for (int bb = 0; bb < kBatch; ++bb) {
+            cur[bb] = nxt[bb];
+            csc[bb] = nsc[bb];
           }
         }
+        }
+        if (ptid < kTile) sm.rec[(tile + 2) % 3][ptid] = rec_of(j_ahead, blk_ahead);
         fence_proxy_async();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.kv_full);
-        named_bar_sync(2, kProducerThreads);  // next tile's addresses complete; this tile's reads done
+        if (lane == 0) mbar_arrive(&sm.kv_full[kb]);
+        named_bar_sync(2, kProducerThreads);  // tile t+2's addresses complete; this tile's reads done
       }
       if (!ok) break;
       ++nw;
@@ -379,12 +471,25 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
     if (lane == 0) {
       uint32_t n = 0, nw = 0, kk = 0;
       bool issued = false;
-      const uint32_t idesc1 = make_idesc(128, kHeads, 1, 1, 0, 0);  // bf16, both K-major
-      const uint32_t idesc2 = make_idesc(128, kHeads, 1, 1, 1, 1);  // bf16, both MN-major
-      const int dtiles = (DL + 127) / 128;
-      const uint32_t kv0 = smem_u32(sm.kv[0]);
+      const uint32_t idesc1 = make_idesc(kTile, kHeads, 1, 1, 0, 0);  // bf16, both K-major, M = 64 keys
+      const uint32_t idesc2 = make_idesc(128, kHeads, 1, 1, 1, 1);    // bf16, both MN-major, M = 128 dims
       const uint32_t q0 = smem_u32(sm.q[0]);
-      const uint32_t pt = smem_u32(sm.kv[kLatChunks]);
+      // MMA2 of global tile k2: O^T += V^T . P^T over the tile's 64 keys.
+      const auto mma2 = [&](uint32_t k2, bool first) -> bool {
+        const int b2 = k2 & 1;
+        if (!mbar_wait(&sm.p_full[b2], (k2 >> 1) & 1, A.err, abort)) return false;
+        tc_fence_after();
+        const uint32_t kv0 = smem_u32(sm.kv[b2][0]);
+        const uint32_t pt = smem_u32(sm.kv[b2][kLatChunks]);
+        for (int d2 = 0; d2 < kDTiles; ++d2) {
+          for (int k16 = 0; k16 < kTile / 16; ++k16) {
+            mma_f16(tmem_o + d2 * kHeads, sw128_desc(kv0 + 2 * d2 * kChunkBytes + k16 * 2048, kChunkBytes, 1024),
+                    sw128_desc(pt + k16 * 2048, kChunkBytes, 1024), idesc2, !(first && k16 == 0));
+          }
+        }
+        mma_commit(&sm.kv_empty[b2]);
+        return true;
+      };
       for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
         if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
         const int ntiles = sm.ntiles[n & 1];
@@ -393,47 +498,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         if (!mbar_wait(&sm.q_full, nw & 1, A.err, abort)) break;
         bool ok = true;
         for (int tile = 0; tile < ntiles; ++tile, ++kk) {
-          if (!mbar_wait(&sm.kv_full, kk & 1, A.err, abort)) {
+          const int kb = kk & 1;
+          // MMA2 of the previous tile first: it releases that tile's buffer to the producers,
+          // which must not wait for this tile's gather.
+          if (tile > 0 && !mma2(kk - 1, tile == 1)) {
+            ok = false;
+            break;
+          }
+          if (!mbar_wait(&sm.kv_full[kb], (kk >> 1) & 1, A.err, abort) ||
+              !mbar_wait(&sm.s_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort)) {
             ok = false;
             break;
           }
           tc_fence_after();
+          const uint32_t kv0 = smem_u32(sm.kv[kb][0]);
           for (int c = 0; c < NCH; ++c) {
             for (int k4 = 0; k4 < 4; ++k4) {
-              mma_f16(tmem_s, sw128_desc(kv0 + c * kTile * 128 + k4 * 32, 16, 1024),
+              mma_f16(tmem_s + kb * kHeads, sw128_desc(kv0 + c * kChunkBytes + k4 * 32, 16, 1024),
                       sw128_desc(q0 + c * kHeads * 128 + k4 * 32, 16, 1024), idesc1, (c | k4) != 0);
             }
           }
           issued = true;
-          mma_commit(&sm.s_full);
+          mma_commit(&sm.s_full[kb]);
           if (tile == ntiles - 1) mma_commit(&sm.q_empty);
-          if (!mbar_wait(&sm.p_full, kk & 1, A.err, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          for (int d2 = 0; d2 < dtiles; ++d2) {
-            for (int k8 = 0; k8 < kTile / 16; ++k8) {
-              mma_f16(tmem_o + d2 * kHeads, sw128_desc(kv0 + 2 * d2 * kTile * 128 + k8 * 2048, kTile * 128, 1024),
-                      sw128_desc(pt + k8 * 2048, kTile * 128, 1024), idesc2, (tile | k8) != 0);
-            }
-          }
-          mma_commit(&sm.kv_empty);
-          if (tile == ntiles - 1) mma_commit(&sm.o_done);
         }
-        if (!ok) break;
+        if (!ok || !mma2(kk - 1, ntiles == 1)) break;
+        mma_commit(&sm.o_done);
         ++nw;
       }
       if (issued) {
         mma_commit(&sm.final_bar);
-        mbar_wait(&sm.final_bar, 0, A.err, abort);
+        mbar_drain(&sm.final_bar, 0);
       }
     }
   } else {
-    // ------------------------------ softmax + epilogue (warps 0-3) ------------------------------
+    // ------------------------------ softmax + epilogue (warps 0-7) ------------------------------
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kSoftmaxRegs));
-    const int tid = threadIdx.x;  // key row of the tile / dim row of an O^T tile
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    const int tid = threadIdx.x;            // 0..255
+    const int sp = warp & 3;                // TMEM sub-partition
+    const int hh = warp >> 2;               // head half: heads 32 hh .. 32 hh + 31
+    const int key = 16 * sp + lane;         // key of the tile (lanes < 16)
+    const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
     uint32_t n = 0, nw = 0, kk = 0;
     for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
       const int t = A.tok_begin + tr;
@@ -442,40 +547,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tok_empty[n & 1]);
       if (ntiles == 0) {
-        for (int i = tid; i < A.n_heads * DL; i += 128)
+        for (int i = tid; i < A.n_heads * DL; i += kSoftmaxThreads)
           A.out[static_cast<int64_t>(t) * A.n_heads * DL + i] = __float2bfloat16(0.f);
         if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = -INFINITY;
         continue;
       }
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
-      float l_part[kHeads];
+      float l_part[32];
 #pragma unroll
-      for (int h = 0; h < kHeads; ++h) l_part[h] = 0.f;
+      for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
       bool ok = true;
       for (int tile = 0; tile < ntiles; ++tile, ++kk) {
-        const int e = tile * kTile + tid;
-        const bool valid = e < A.top_k && __ldg(idx + e) >= 0;
-        if (!mbar_wait(&sm.s_full, kk & 1, A.err, abort)) {
+        const int kb = kk & 1;
+        const int e = tile * kTile + key;
+        const bool valid = lane < 16 && e < A.top_k && __ldg(idx + e) >= 0;
+        if (!mbar_wait(&sm.s_full[kb], (kk >> 1) & 1, A.err, abort)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        // per-head maximum of this tile
+        float sc[32];
         {
-          float v[kHeads];
+          uint32_t r[32];
+          tmem_ld32(tmem_s + lane_base + kb * kHeads + 32 * hh, r);
+          tmem_ld_wait();
 #pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            uint32_t r[32];
-            tmem_ld32(tmem_s + lane_base + 32 * half, r);
-            tmem_ld_wait();
-#pragma unroll
-            for (int h = 0; h < 32; ++h) v[32 * half + h] = valid ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
-          }
-          warp_transpose_reduce<true>(v, lane);
-          sm.red[warp][2 * lane] = v[0];
-          sm.red[warp][2 * lane + 1] = v[1];
+          for (int h = 0; h < 32; ++h) sc[h] = valid ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
         }
-        named_bar_sync(1, 128);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sm.s_empty[kb]);  // the scores are in registers
+        // per-head maximum of this tile over the warp's keys; lane h keeps head 32 hh + h
+        {
+          float mine = -INFINITY;
+#pragma unroll
+          for (int h = 0; h < 32; ++h) {
+            const float m = warp_max(sc[h]);
+            mine = lane == h ? m : mine;
+          }
+          sm.red[sp][32 * hh + lane] = mine;
+        }
+        named_bar_sync(1, kSoftmaxThreads);
         int need_h = 0;
         if (tid < kHeads) {
           const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
@@ -483,101 +595,99 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           need_h = tile == 0 || mt > sm.m_run[tid] + kRescaleThreshold;
         }
         // one barrier that also ORs the per-head "running max must move" flags
-        if (bar_red_or(1, 128, need_h)) {
+        const bool moved = bar_red_or(1, kSoftmaxThreads, need_h) != 0;
+        if (moved) {
           if (tid < kHeads) {
             const float old = tile == 0 ? -INFINITY : sm.m_run[tid];
             const float mn = fmaxf(old, sm.m_tile[tid]);
             sm.alpha[tid] = (tile == 0 || mn == -INFINITY) ? 1.f : exp2f(old - mn);
             sm.m_run[tid] = mn;
           }
-          named_bar_sync(1, 128);
+          named_bar_sync(1, kSoftmaxThreads);
           if (tile > 0) {
 #pragma unroll
-            for (int h = 0; h < kHeads; ++h) l_part[h] *= sm.alpha[h];
-            const int dtiles = (DL + 127) / 128;
-#pragma unroll 1
-            for (int d2 = 0; d2 < dtiles; ++d2) {
-#pragma unroll 1
-              for (int hh = 0; hh < kHeads; hh += 32) {
-                uint32_t o[32];
-                tmem_ld32(tmem_o + lane_base + d2 * kHeads + hh, o);
-                tmem_ld_wait();
-#pragma unroll
-                for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * sm.alpha[hh + x]);
-                tmem_st32(tmem_o + lane_base + d2 * kHeads + hh, o);
-              }
-            }
-            tmem_st_wait();
+            for (int h = 0; h < 32; ++h) l_part[h] *= sm.alpha[32 * hh + h];
           }
         }
-        // probabilities -> bf16 P^T row (this key) in the rope chunk
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          uint32_t r[32];
-          tmem_ld32(tmem_s + lane_base + 32 * half, r);
-          tmem_ld_wait();
+        // probabilities -> bf16 P^T row (this key, this warp's 32 heads) in the rope chunk
+        {
           uint32_t pw[16];
 #pragma unroll
           for (int hx = 0; hx < 32; hx += 2) {
-            const int h = 32 * half + hx;
+            const int h = 32 * hh + hx;
             const float m0 = sm.m_run[h], m1 = sm.m_run[h + 1];
-            const float s0 = valid ? __uint_as_float(r[hx]) * A.scale_log2 : -INFINITY;
-            const float s1 = valid ? __uint_as_float(r[hx + 1]) * A.scale_log2 : -INFINITY;
-            const float p0 = fast_exp2(s0 - (m0 == -INFINITY ? 0.f : m0));
-            const float p1 = fast_exp2(s1 - (m1 == -INFINITY ? 0.f : m1));
+            const float p0 = fast_exp2(sc[hx] - (m0 == -INFINITY ? 0.f : m0));
+            const float p1 = fast_exp2(sc[hx + 1] - (m1 == -INFINITY ? 0.f : m1));
             const __nv_bfloat162 pb = __floats2bfloat162_rn(p0, p1);
             const float2 pf = __bfloat1622float2(pb);
-            l_part[h] += pf.x;
-            l_part[h + 1] += pf.y;
+            l_part[hx] += pf.x;
+            l_part[hx + 1] += pf.y;
             pw[hx / 2] = (static_cast<uint32_t>(__bfloat16_as_ushort(pb.y)) << 16) | __bfloat16_as_ushort(pb.x);
           }
+          if (lane < 16) {
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            *reinterpret_cast<uint4*>(&sm.kv[kLatChunks][sw128_off(tid, 4 * half + v)]) =
-                make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+            for (int v = 0; v < 4; ++v) {
+              *reinterpret_cast<uint4*>(&sm.kv[kb][kLatChunks][sw128_off(key, 4 * hh + v)]) =
+                  make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
+            }
           }
+        }
+        // rescale O^T when a running max moved; it holds MMA2 of the previous tile once that
+        // tile's buffer was released, and MMA2 of this tile waits for p_full below
+        if (moved && tile > 0) {
+          const uint32_t kp = kk - 1;
+          if (!mbar_wait(&sm.kv_empty[kp & 1], (kp >> 1) & 1, A.err, abort)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+#pragma unroll 1
+          for (int d2 = 0; d2 < kDTiles; ++d2) {
+            uint32_t o[32];
+            tmem_ld32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * sm.alpha[32 * hh + x]);
+            tmem_st32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
+          }
+          tmem_st_wait();
         }
         fence_proxy_async();
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&sm.p_full);
+        if (lane == 0) mbar_arrive(&sm.p_full[kb]);
       }
       if (!ok) break;
       // ---- end of token: row sums, normalisation, lse ----
       if (!mbar_wait(&sm.o_done, nw & 1, A.err, abort)) break;
       tc_fence_after();
-      warp_transpose_reduce<false>(l_part, lane);
-      sm.red[warp][2 * lane] = l_part[0];
-      sm.red[warp][2 * lane + 1] = l_part[1];
-      named_bar_sync(1, 128);
+      warp_transpose_reduce32<false>(l_part, lane);
+      sm.red[sp][32 * hh + lane] = l_part[0];
+      named_bar_sync(1, kSoftmaxThreads);
       if (tid < kHeads) {
         const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
         sm.l_fin[tid] = l;
         if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = (sm.m_run[tid] + log2f(l)) * kLn2;
       }
-      named_bar_sync(1, 128);
-      const int dtiles = (DL + 127) / 128;
+      named_bar_sync(1, kSoftmaxThreads);
 #pragma unroll 1
-      for (int d2 = 0; d2 < dtiles; ++d2) {
-        const int d = d2 * 128 + tid;
-#pragma unroll 1
-        for (int hh = 0; hh < kHeads; hh += 32) {
-          uint32_t o[32];
-          tmem_ld32(tmem_o + lane_base + d2 * kHeads + hh, o);
-          tmem_ld_wait();
-          if (d < DL) {
+      for (int d2 = 0; d2 < kDTiles; ++d2) {
+        const int d = d2 * 128 + sp * 32 + lane;
+        uint32_t o[32];
+        tmem_ld32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
+        tmem_ld_wait();
+        if (d < DL) {
 #pragma unroll
-            for (int x = 0; x < 32; ++x) {
-              const int h = hh + x;
-              if (h < A.n_heads)
-                A.out[(static_cast<int64_t>(t) * A.n_heads + h) * DL + d] =
-                    __float2bfloat16(__uint_as_float(o[x]) / sm.l_fin[h]);
-            }
+          for (int x = 0; x < 32; ++x) {
+            const int h = 32 * hh + x;
+            if (h < A.n_heads)
+              A.out[(static_cast<int64_t>(t) * A.n_heads + h) * DL + d] =
+                  __float2bfloat16(__uint_as_float(o[x]) / sm.l_fin[h]);
           }
         }
       }
       tc_fence_before();
-      named_bar_sync(1, 128);  // l_fin / m_run reused by the next token
+      named_bar_sync(1, kSoftmaxThreads);  // l_fin / m_run reused by the next token
       ++nw;
     }
   }
@@ -590,23 +700,23 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
   }
 }
 
-template <int NCH>
+template <int NCH, bool WR>
 smla_status_t launch_nch(const AttnArgs& A, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem<NCH>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attend_kernel<NCH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attend_kernel<NCH, WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     // setmaxnreg.inc can only draw on the registers the CTA was launched with;
     // refuse to launch if the compiled allocation does not cover the split.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH>) != cudaSuccess) return SMLA_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH, WR>) != cudaSuccess) return SMLA_ERR_CUDA;
     if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set = true;
   }
   const int grid = min(A.n_rows, device_sm_count());
-  attend_kernel<NCH><<<grid, kThreads, smem, stream>>>(A);
+  attend_kernel<NCH, WR><<<grid, kThreads, smem, stream>>>(A);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
@@ -638,8 +748,12 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
   A.lse = lse;
   A.err = err;
   switch (L.d_latent / 64) {
-    case 1: return launch_nch<2>(A, stream);
-    case 8: return launch_nch<9>(A, stream);
+    case 1: return launch_nch<2, false>(A, stream);
+    case 8: {
+      // records of 512 codes, four per-128 scales and 64 rope values take the whole-record gather
+      const bool wr = L.n_scales == 4 && L.quant_tile == 128 && L.d_rope == 64 && (512 + 4 * L.n_scales) % 16 == 0;
+      return wr ? launch_nch<9, true>(A, stream) : launch_nch<9, false>(A, stream);
+    }
     default: return SMLA_ERR_UNSUPPORTED;
   }
 }
