@@ -27,8 +27,9 @@
 //   * MMA2: O^T[dim, head] += V^T[dim, key] . P^T[key, head] with both operands
 //     MN-major: the same swizzled latent chunks serve as V^T without a
 //     transpose; M = 128 dims x 4 tiles, N = 64 heads, K = 64 keys.  The MMA
-//     warp issues MMA2 of tile t-1 as soon as its probabilities are ready (it
-//     releases that buffer to the producers), then MMA1 of tile t once gathered.
+//     warp polls both: MMA2 of a tile as soon as its probabilities are written
+//     (it releases that buffer to the producers), MMA1 of the next tile as soon
+//     as it is gathered (the next scores are computed while the softmax works).
 //   * Epilogue: O^T / l -> bf16 out[t, h, d] (thread = dim, coalesced) and
 //     lse = ln(sum) from the running max and the reduced row sums.
 #include "smla_internal.h"
@@ -107,6 +108,18 @@ __device__ __forceinline__ void warp_transpose_reduce32(float (&v)[32], int lane
       v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
     }
   }
+}
+
+// Non-blocking test of the phase of `bar` with the given parity.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // Maximum of v over the 32 lanes (every lane receives it).
@@ -474,11 +487,21 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       const uint32_t idesc1 = make_idesc(kTile, kHeads, 1, 1, 0, 0);  // bf16, both K-major, M = 64 keys
       const uint32_t idesc2 = make_idesc(128, kHeads, 1, 1, 1, 1);    // bf16, both MN-major, M = 128 dims
       const uint32_t q0 = smem_u32(sm.q[0]);
+      // MMA1 of global tile k1: S^T = Khat . q^T over 576 dims into S buffer k1 % 2.
+      const auto mma1 = [&](uint32_t k1) {
+        const int b1 = k1 & 1;
+        const uint32_t kv0 = smem_u32(sm.kv[b1][0]);
+        for (int c = 0; c < NCH; ++c) {
+          for (int k4 = 0; k4 < 4; ++k4) {
+            mma_f16(tmem_s + b1 * kHeads, sw128_desc(kv0 + c * kChunkBytes + k4 * 32, 16, 1024),
+                    sw128_desc(q0 + c * kHeads * 128 + k4 * 32, 16, 1024), idesc1, (c | k4) != 0);
+          }
+        }
+        mma_commit(&sm.s_full[b1]);
+      };
       // MMA2 of global tile k2: O^T += V^T . P^T over the tile's 64 keys.
-      const auto mma2 = [&](uint32_t k2, bool first) -> bool {
+      const auto mma2 = [&](uint32_t k2, bool first) {
         const int b2 = k2 & 1;
-        if (!mbar_wait(&sm.p_full[b2], (k2 >> 1) & 1, A.err, abort)) return false;
-        tc_fence_after();
         const uint32_t kv0 = smem_u32(sm.kv[b2][0]);
         const uint32_t pt = smem_u32(sm.kv[b2][kLatChunks]);
         for (int d2 = 0; d2 < kDTiles; ++d2) {
@@ -488,7 +511,6 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           }
         }
         mma_commit(&sm.kv_empty[b2]);
-        return true;
       };
       for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
         if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
@@ -496,33 +518,47 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         mbar_arrive(&sm.tok_empty[n & 1]);
         if (ntiles == 0) continue;
         if (!mbar_wait(&sm.q_full, nw & 1, A.err, abort)) break;
+        // Issue whichever is ready: MMA2 of the oldest tile whose probabilities are written
+        // (it releases that tile buffer to the producers), else MMA1 of the next gathered tile
+        // (so the next scores are computed while the softmax works).
+        const uint32_t kbeg = kk, kend = kk + ntiles;
+        uint32_t k1 = kbeg, k2 = kbeg;
+        uint64_t t_last = globaltimer_ns();
         bool ok = true;
-        for (int tile = 0; tile < ntiles; ++tile, ++kk) {
-          const int kb = kk & 1;
-          // MMA2 of the previous tile first: it releases that tile's buffer to the producers,
-          // which must not wait for this tile's gather.
-          if (tile > 0 && !mma2(kk - 1, tile == 1)) {
-            ok = false;
-            break;
+        while (k2 < kend) {
+          bool progress = false;
+          if (k2 < k1 && mbar_test(&sm.p_full[k2 & 1], (k2 >> 1) & 1)) {
+            tc_fence_after();
+            mma2(k2, k2 == kbeg);
+            ++k2;
+            progress = true;
+          } else if (k1 < kend && mbar_test(&sm.kv_full[k1 & 1], (k1 >> 1) & 1) &&
+                     mbar_test(&sm.s_empty[k1 & 1], ((k1 >> 1) & 1) ^ 1)) {
+            tc_fence_after();
+            mma1(k1);
+            issued = true;
+            if (k1 == kend - 1) mma_commit(&sm.q_empty);
+            ++k1;
+            progress = true;
           }
-          if (!mbar_wait(&sm.kv_full[kb], (kk >> 1) & 1, A.err, abort) ||
-              !mbar_wait(&sm.s_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t kv0 = smem_u32(sm.kv[kb][0]);
-          for (int c = 0; c < NCH; ++c) {
-            for (int k4 = 0; k4 < 4; ++k4) {
-              mma_f16(tmem_s + kb * kHeads, sw128_desc(kv0 + c * kChunkBytes + k4 * 32, 16, 1024),
-                      sw128_desc(q0 + c * kHeads * 128 + k4 * 32, 16, 1024), idesc1, (c | k4) != 0);
+          if (progress) {
+            t_last = globaltimer_ns();
+          } else {
+            if (*abort) {
+              ok = false;
+              break;
             }
+            if (globaltimer_ns() - t_last > kWaitLimitNs) {
+              latch_error(A.err, SMLA_ERR_TIMEOUT);
+              *abort = 1;
+              ok = false;
+              break;
+            }
+            __nanosleep(20);
           }
-          issued = true;
-          mma_commit(&sm.s_full[kb]);
-          if (tile == ntiles - 1) mma_commit(&sm.q_empty);
         }
-        if (!ok || !mma2(kk - 1, ntiles == 1)) break;
+        kk = kend;
+        if (!ok) break;
         mma_commit(&sm.o_done);
         ++nw;
       }
