@@ -64,7 +64,7 @@ struct __align__(1024) AttnSmem {
   float m_tile[kHeads];
   float m_run[kHeads];
   float alpha[kHeads];
-  float l_fin[kHeads];
+  float l_fin[kHeads];              // 1 / row sum per head
   int ntiles[2];
   uint64_t tok_full[2], tok_empty[2];
   uint64_t q_full, q_empty;
@@ -469,10 +469,11 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           }
         }
         }
-        if (ptid < kTile) sm.rec[(tile + 2) % 3][ptid] = rec_of(j_ahead, blk_ahead);
         fence_proxy_async();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.kv_full[kb]);
+        // tile t+2's addresses after the hand-off: the block-table load must not delay the MMA
+        if (ptid < kTile) sm.rec[(tile + 2) % 3][ptid] = rec_of(j_ahead, blk_ahead);
         named_bar_sync(2, kProducerThreads);  // tile t+2's addresses complete; this tile's reads done
       }
       if (!ok) break;
@@ -702,7 +703,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       named_bar_sync(1, kSoftmaxThreads);
       if (tid < kHeads) {
         const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
-        sm.l_fin[tid] = l;
+        sm.l_fin[tid] = 1.f / l;  // normalisation as one reciprocal per head
         if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = (sm.m_run[tid] + log2f(l)) * kLn2;
       }
       named_bar_sync(1, kSoftmaxThreads);
@@ -718,7 +719,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
             const int h = 32 * hh + x;
             if (h < A.n_heads)
               A.out[(static_cast<int64_t>(t) * A.n_heads + h) * DL + d] =
-                  __float2bfloat16(__uint_as_float(o[x]) / sm.l_fin[h]);
+                  __float2bfloat16(__uint_as_float(o[x]) * sm.l_fin[h]);
           }
         }
       }
