@@ -6,19 +6,21 @@
 //
 // One CTA per query row; scores map to order-preserving 32-bit keys (-0 folded
 // onto +0).  Fast path, one coalesced read of the row:
-//   1. an 8,192-element strided sample (runs of 4) is radix-selected in shared
-//      memory to a threshold T whose rank in the sample leaves a safety margin
-//      above k/n of the sample;
-//   2. every element with key >= T is collected as a 64-bit (key, ~position)
-//      pair in shared memory (warp-aggregated appends, four 16-byte loads in
-//      flight per thread).
-// If at least k and at most the capacity were collected, a radix select over the
-// candidates gives the exact k-th largest key; keys above it are kept, ties keep
-// their lowest positions, and a bitonic sort of the k kept positions writes
-// them in ascending order.  Rows
-// with at most `capacity` positions take every position as a candidate.
-// Otherwise the row falls back to a radix select over all 32 key bits (three
-// histogram passes) and an index-ordered selection pass.
+//   1. an 8,192-element strided sample (runs of 4) is radix-selected (top 24 key
+//      bits) in shared memory to a threshold T whose rank in the sample leaves a
+//      safety margin above k/n of the sample;
+//   2. warp w scans its own contiguous segment of the row and appends every
+//      element with key >= T, as a 64-bit (key, ~position) pair, to its own list
+//      in shared memory, in position order (16 keys per lane per iteration, the
+//      next 16 in flight; one warp scan per iteration places the hits).
+// If at least k were collected and no list overflowed, a radix select over the
+// lists gives the exact k-th largest key; keys above it are kept and ties keep
+// their lowest positions.  Because the lists are position-ordered and the
+// segments increase with the warp index, every warp writes its kept positions
+// straight to their output slots from per-warp prefix counts: the output is in
+// ascending order without a sort.  Rows with at most `capacity` positions take
+// every position as a candidate.  Otherwise the row falls back to a radix select
+// over all 32 key bits (three histogram passes) and an index-ordered selection.
 #include "smla_internal.h"
 
 namespace smla {
@@ -30,13 +32,15 @@ constexpr int kBins = 4096;
 constexpr int kCap = 8192;     // candidate capacity of the fast path (power of two)
 constexpr int kSample = 8192;  // sample size for the threshold (runs of 4)
 constexpr int kMaxK = 4096;    // largest k of the fast path (power of two)
+constexpr int kWarpCap = kCap / kWarps;  // candidates per warp list (512)
+constexpr int kSpan = 32 * 16;           // positions a warp scans per iteration (16 per lane)
 
 struct TopkSmem {
   int hist[kBins];
   unsigned long long cand[kCap];
-  int sel[kMaxK];
   int warp_tot[32];
-  int n_sel, n_cand, n_tie, sel_bin, sel_above;
+  int sel_bin, sel_above;
+  int wcnt[kWarps], wgt[kWarps], weq[kWarps];  // per-warp candidate lists: length, > T, == T
 };
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -135,50 +139,16 @@ __device__ __forceinline__ void find_bin(TopkSmem& sm, int nb, int remaining) {
   __syncthreads();
 }
 
-template <typename T, bool kDescending>
-__device__ __forceinline__ void bitonic_sort(T* a, int m) {
-  for (int size = 2; size <= m; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      for (int i = threadIdx.x; i < m / 2; i += kThreads) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool up = ((lo & size) == 0) != kDescending;
-        const T x = a[lo], y = a[hi];
-        if ((x > y) == up) {
-          a[lo] = y;
-          a[hi] = x;
-        }
-      }
-      __syncthreads();
-    }
-  }
-}
-
-// Warp-aggregated append of `v` to list[counter++] for the lanes with `pred`.
-template <typename T>
-__device__ __forceinline__ void warp_append(bool pred, T v, T* list, int* counter, int cap) {
-  const uint32_t m = __ballot_sync(0xffffffffu, pred);
-  if (m == 0) return;
-  const int lane = threadIdx.x & 31;
-  const int leader = __ffs(m) - 1;
-  int base = 0;
-  if (lane == leader) base = atomicAdd(counter, __popc(m));
-  base = __shfl_sync(0xffffffffu, base, leader);
-  if (pred) {
-    const int pos = base + __popc(m & ((1u << lane) - 1u));
-    if (pos < cap) list[pos] = v;
-  }
-}
-
 // The want-th largest of n keys in shared memory (radix select on 12, 12, 8
-// bits).  `rem` returns how many keys equal to the result are within the top
+// bits; `passes` < 3 stops early and returns the prefix of the decided bits).  `rem`
+// returns how many keys equal to the result are within the top
 // `want` (1 <= rem <= count of that key).
-__device__ uint32_t radix_select(TopkSmem& sm, const uint32_t* keys, int n, int want, int& rem) {
+__device__ uint32_t radix_select(TopkSmem& sm, const uint32_t* keys, int n, int want, int& rem, int passes = 3) {
   uint32_t prefix = 0, mask = 0;
   int remaining = want;
   const int shifts[3] = {20, 8, 0};
   const int widths[3] = {12, 12, 8};
-  for (int pass = 0; pass < 3; ++pass) {
+  for (int pass = 0; pass < passes; ++pass) {
     const int shift = shifts[pass];
     const uint32_t bmask = (1u << widths[pass]) - 1u;
     const int nb = 1 << widths[pass];
@@ -199,8 +169,10 @@ __device__ uint32_t radix_select(TopkSmem& sm, const uint32_t* keys, int n, int 
   return prefix;
 }
 
-// The k-th largest key among the packed (key << 32 | ~position) candidates.
-__device__ uint32_t radix_select_cand(TopkSmem& sm, int n, int k, int& rem) {
+// The k-th largest key among the per-warp candidate lists (warp w's list is
+// cand[w * kWarpCap .. + wcnt[w])).
+// `mask_out` gives the key bits the result decides: compare (key & mask_out) with it.
+__device__ uint32_t radix_select_lists(TopkSmem& sm, int k, int& rem, uint32_t& mask_out) {
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
   const int shifts[3] = {20, 8, 0};
@@ -211,19 +183,22 @@ __device__ uint32_t radix_select_cand(TopkSmem& sm, int n, int k, int& rem) {
     const int nb = 1 << widths[pass];
     for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
     __syncthreads();
-    for (int base = 0; base < n; base += kThreads) {
-      const int i = base + threadIdx.x;
-      const uint32_t key = i < n ? static_cast<uint32_t>(sm.cand[i] >> 32) : 0u;
-      add_to_hist(sm.hist, key, i < n, mask, prefix, shift, bmask);
+    for (int i = threadIdx.x; i < kCap; i += kThreads) {
+      const bool in = (i % kWarpCap) < sm.wcnt[i / kWarpCap];
+      const uint32_t key = in ? static_cast<uint32_t>(sm.cand[i] >> 32) : 0u;
+      add_to_hist(sm.hist, key, in, mask, prefix, shift, bmask);
     }
     __syncthreads();
     find_bin(sm, nb, remaining);
     remaining -= sm.sel_above;
     prefix |= static_cast<uint32_t>(sm.sel_bin) << shift;
     mask |= bmask << shift;
+    const bool exact = sm.hist[sm.sel_bin] == remaining;
     __syncthreads();
+    if (exact) break;  // every key of the bin is taken: the prefix already separates them
   }
   rem = remaining;
+  mask_out = mask;
   return prefix;
 }
 
@@ -312,135 +287,135 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     const int want = min(kSample, r + 4 * static_cast<int>(sqrtf(static_cast<float>(r))) + 16);
     __syncthreads();
     int rem;
-    thr = radix_select(sm, samp, kSample, want, rem);
+    thr = radix_select(sm, samp, kSample, want, rem, 2);  // 24 bits: the threshold's bin is kept whole
   }
-  if (threadIdx.x == 0) sm.n_cand = 0;
-  __syncthreads();
-  // ---- one pass: collect every key >= thr (four 16-byte loads in flight per thread) ----
-  const auto collect = [&](int j, float x, bool in) {
-    const uint32_t key = order_key(x);
-    warp_append<unsigned long long>(in && key >= thr,
-                                    (static_cast<unsigned long long>(key) << 32) | static_cast<uint32_t>(~j), sm.cand,
-                                    &sm.n_cand, kCap);
-  };
-  if ((reinterpret_cast<uintptr_t>(s) & 15) == 0) {
-    // Each iteration a thread holds U float4 (16 keys); the next iteration's loads are issued
-    // before this one is filtered.  A warp reserves room for all its hits with one atomic.
-    constexpr int U = 4;
-    const int lane = threadIdx.x & 31;
-    const int n4 = (n + 3) / 4;
-    const int span = kThreads * U;
-    const int bound = (n4 + span - 1) / span * span;
-    const auto load = [&](int base, float4 (&v)[U]) {
+  if ((reinterpret_cast<uintptr_t>(s) & 15) != 0) {  // rows that are not 16-byte aligned
+    topk_slow(sm, s, n, k, o);
+    return;
+  }
+  // ---- one pass: warp w scans its own contiguous segment and appends every key >= thr, in
+  // position order, to its own list (16 keys per lane per iteration, the next 16 in flight) ----
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (n + kWarps * kSpan - 1) / (kWarps * kSpan) * kSpan;
+  const int p_lo = min(n, warp * seg), p_hi = min(n, p_lo + seg);
+  unsigned long long* list = sm.cand + warp * kWarpCap;
+  const auto load = [&](int p0, float4 (&v)[4]) {
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = 4 * (base + u * kThreads);
-        if (j + 3 < n) {
-          v[u] = __ldg(reinterpret_cast<const float4*>(s + j));
-        } else {
-          v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
-          if (j < n) v[u].x = __ldg(s + j);
-          if (j + 1 < n) v[u].y = __ldg(s + j + 1);
-          if (j + 2 < n) v[u].z = __ldg(s + j + 2);
-        }
+    for (int u = 0; u < 4; ++u) {
+      const int j = p0 + 4 * u;
+      if (j + 3 < p_hi) {
+        v[u] = __ldg(reinterpret_cast<const float4*>(s + j));
+      } else {
+        v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < p_hi) v[u].x = __ldg(s + j);
+        if (j + 1 < p_hi) v[u].y = __ldg(s + j + 1);
+        if (j + 2 < p_hi) v[u].z = __ldg(s + j + 2);
       }
-    };
-    float4 cur[U], nxt[U];
-    load(threadIdx.x, cur);
-    for (int base = threadIdx.x; base < bound; base += span) {
-      if (base + span < bound) load(base + span, nxt);
-      uint32_t keys[4 * U];
+    }
+  };
+  int count = 0;  // warp-uniform length of this warp's list
+  {
+    float4 cur[4], nxt[4];
+    if (p_lo < p_hi) load(p_lo + 16 * lane, cur);
+    for (int base = p_lo; base < p_hi; base += kSpan) {
+      const int p0 = base + 16 * lane;
+      if (base + kSpan < p_hi) load(p0 + kSpan, nxt);
+      uint32_t keys[16];
       uint32_t hit = 0;
 #pragma unroll
-      for (int u = 0; u < U; ++u) {
-        const int j = 4 * (base + u * kThreads);
+      for (int u = 0; u < 4; ++u) {
         keys[4 * u] = order_key(cur[u].x);
         keys[4 * u + 1] = order_key(cur[u].y);
         keys[4 * u + 2] = order_key(cur[u].z);
         keys[4 * u + 3] = order_key(cur[u].w);
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-          if (j + e < n && keys[4 * u + e] >= thr) hit |= 1u << (4 * u + e);
       }
+#pragma unroll
+      for (int e = 0; e < 16; ++e)
+        if (p0 + e < p_hi && keys[e] >= thr) hit |= 1u << e;
       const int cnt = __popc(hit);
       int incl = cnt;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += y;
+      for (int o2 = 1; o2 < 32; o2 <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, incl, o2);
+        if (lane >= o2) incl += y;
       }
-      const int total = __shfl_sync(0xffffffffu, incl, 31);
-      if (total > 0) {
-        int pos = 0;
-        if (lane == 31) pos = atomicAdd(&sm.n_cand, total);
-        pos = __shfl_sync(0xffffffffu, pos, 31) + incl - cnt;
+      int pos = count + incl - cnt;
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            if (hit & (1u << (4 * u + e))) {
-              const int j = 4 * (base + u * kThreads) + e;
-              if (pos < kCap)
-                sm.cand[pos] = (static_cast<unsigned long long>(keys[4 * u + e]) << 32) | static_cast<uint32_t>(~j);
-              ++pos;
-            }
-          }
+      for (int e = 0; e < 16; ++e) {
+        if (hit & (1u << e)) {
+          if (pos < kWarpCap)
+            list[pos] = (static_cast<unsigned long long>(keys[e]) << 32) | static_cast<uint32_t>(~(p0 + e));
+          ++pos;
         }
       }
+      count += __shfl_sync(0xffffffffu, incl, 31);
 #pragma unroll
-      for (int u = 0; u < U; ++u) cur[u] = nxt[u];
+      for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
     }
-  } else {
-    for_row(s, n, collect);
   }
+  if (lane == 0) sm.wcnt[warp] = count;
   __syncthreads();
-  const int n_cand = sm.n_cand;
-  if (n_cand < k || n_cand > kCap) {  // the sample's guess missed: exact radix select over the row
+  int n_cand = 0;
+  bool over = false;
+#pragma unroll
+  for (int w = 0; w < kWarps; ++w) {
+    n_cand += sm.wcnt[w];
+    over |= sm.wcnt[w] > kWarpCap;
+  }
+  if (n_cand < k || over) {  // the sample's guess missed: exact radix select over the row
     topk_slow(sm, s, n, k, o);
     return;
   }
-  // ---- exact k-th largest key T among the candidates, and how many keys == T to keep ----
+  // ---- exact k-th largest key T among the candidates ----
   int need_eq;
-  const uint32_t T = radix_select_cand(sm, n_cand, k, need_eq);
-  // ---- keep key > T, and the need_eq lowest positions among key == T ----
-  if (threadIdx.x == 0) {
-    sm.n_sel = 0;
-    sm.n_tie = 0;
-  }
-  __syncthreads();
-  int* ties = sm.hist;  // free after the radix passes
-  for (int base = 0; base < n_cand; base += kThreads) {
-    const int i = base + threadIdx.x;
-    uint32_t key = 0;
-    int j = 0;
-    if (i < n_cand) {
-      key = static_cast<uint32_t>(sm.cand[i] >> 32);
-      j = static_cast<int>(~static_cast<uint32_t>(sm.cand[i] & 0xFFFFFFFFull));
+  uint32_t tmask;
+  const uint32_t T = radix_select_lists(sm, k, need_eq, tmask);
+  // ---- every warp counts its keys above T and equal to T ----
+  {
+    int gt = 0, eq = 0;
+    for (int j = lane; j < count; j += 32) {
+      const uint32_t key = static_cast<uint32_t>(list[j] >> 32) & tmask;
+      gt += key > T;
+      eq += key == T;
     }
-    warp_append<int>(i < n_cand && key > T, j, sm.sel, &sm.n_sel, kMaxK);
-    warp_append<int>(i < n_cand && key == T, j, ties, &sm.n_tie, kBins);
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o2);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o2);
+    }
+    if (lane == 0) {
+      sm.wgt[warp] = gt;
+      sm.weq[warp] = eq;
+    }
   }
   __syncthreads();
-  const int n_tie = sm.n_tie;
-  if (n_tie > kBins) {  // more equal keys than the tie buffer holds
-    topk_slow(sm, s, n, k, o);
-    return;
+  // ---- lists are in position order and warps cover increasing segments: each warp writes its
+  // kept positions straight to their output slots (ties keep the lowest positions) ----
+  int eq_before = 0, out_off = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int take = max(0, min(sm.weq[w], need_eq - eq_before));
+    eq_before += sm.weq[w];
+    out_off += sm.wgt[w] + take;
   }
-  if (n_tie > need_eq) {  // keep the lowest positions among the ties
-    int mt = 1;
-    while (mt < n_tie) mt <<= 1;
-    for (int i = n_tie + threadIdx.x; i < mt; i += kThreads) ties[i] = 0x7FFFFFFF;
-    __syncthreads();
-    bitonic_sort<int, false>(ties, mt);
+  const int take_eq = max(0, min(sm.weq[warp], need_eq - eq_before));
+  int written = 0, ties_seen = 0;
+  for (int j0 = 0; j0 < count; j0 += 32) {
+    const int j = j0 + lane;
+    uint32_t key = 0;
+    int pos = 0;
+    if (j < count) {
+      key = static_cast<uint32_t>(list[j] >> 32) & tmask;
+      pos = static_cast<int>(~static_cast<uint32_t>(list[j] & 0xFFFFFFFFull));
+    }
+    const bool is_eq = j < count && key == T;
+    const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t below = (1u << lane) - 1u;
+    const bool keep = j < count && (key > T || (is_eq && ties_seen + __popc(eq_mask & below) < take_eq));
+    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+    if (keep) o[out_off + written + __popc(keep_mask & below)] = pos;
+    written += __popc(keep_mask);
+    ties_seen += __popc(eq_mask);
   }
-  const int gt = sm.n_sel;
-  for (int i = threadIdx.x; i < need_eq; i += kThreads) sm.sel[gt + i] = ties[i];
-  int kp = 1;
-  while (kp < k) kp <<= 1;
-  for (int i = k + threadIdx.x; i < kp; i += kThreads) sm.sel[i] = 0x7FFFFFFF;
-  __syncthreads();
-  bitonic_sort<int, false>(sm.sel, kp);
-  for (int i = threadIdx.x; i < k; i += kThreads) o[i] = sm.sel[i];
 }
 
 }  // namespace
