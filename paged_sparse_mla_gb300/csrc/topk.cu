@@ -183,10 +183,16 @@ __device__ uint32_t radix_select_lists(TopkSmem& sm, int k, int& rem, uint32_t& 
     const int nb = 1 << widths[pass];
     for (int i = threadIdx.x; i < nb; i += kThreads) sm.hist[i] = 0;
     __syncthreads();
-    for (int i = threadIdx.x; i < kCap; i += kThreads) {
-      const bool in = (i % kWarpCap) < sm.wcnt[i / kWarpCap];
-      const uint32_t key = in ? static_cast<uint32_t>(sm.cand[i] >> 32) : 0u;
-      add_to_hist(sm.hist, key, in, mask, prefix, shift, bmask);
+    {  // each warp histograms its own list
+      const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+      const int cnt = sm.wcnt[warp];
+      const unsigned long long* list = sm.cand + warp * kWarpCap;
+      for (int j0 = 0; j0 < cnt; j0 += 32) {
+        const int j = j0 + lane;
+        const bool in = j < cnt;
+        const uint32_t key = in ? static_cast<uint32_t>(list[j] >> 32) : 0u;
+        add_to_hist(sm.hist, key, in, mask, prefix, shift, bmask);
+      }
     }
     __syncthreads();
     find_bin(sm, nb, remaining);
