@@ -46,6 +46,21 @@ def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)), int(os.environ.get("WORLD_SIZE", 1))
 
 
+def max_over_ranks(value, world, device="cuda"):
+    """The largest of every rank's value (all ranks receive it); the value itself at world 1."""
+    if world <= 1:
+        return value
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank, world, steps, ms):
+    """Units processed by all ranks per second over `steps` steps that took `ms` (max over ranks)."""
+    return world * units_per_rank * steps / (ms / 1e3)
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -251,16 +266,12 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
-    ms = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms = float(tt.item())
+    ms = max_over_ranks(e0.elapsed_time(e1), world)
     err = smla.smla_get_last_error()
     if err != 0:
         raise RuntimeError(f"device error in the timed region: {smla.status_string(err)}")
     ms_step = ms / args.steps
-    value = world * T * args.steps / (ms / 1e3)
+    value = whole_job_rate(T, world, args.steps, ms)
 
     # ---------------- per-kernel timing: same kernels, separate calls, events on the launch stream ----------------
     kern = {k: [] for k in ("kvpack_store", "smla_index_scores", "smla_topk", "smla_attend")}
@@ -320,12 +331,8 @@ def run_gpu(args):
         e2e_step()
     e1.record(stream)
     torch.cuda.synchronize()
-    ms_e2e = e0.elapsed_time(e1)
-    if world > 1:
-        tt = torch.tensor([ms_e2e], device="cuda")
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_e2e = float(tt.item())
-    e2e_value = world * T * args.steps / (ms_e2e / 1e3)
+    ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = whole_job_rate(T, world, args.steps, ms_e2e)
 
     if rank != 0:
         dist.destroy_process_group()
