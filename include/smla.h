@@ -203,6 +203,29 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
                           void* stream);
 
 /*
+ * smla_prefill_chunk -- chunked prefill on a cached prefix, one layer
+ * ([GLM-5.3 "Config and numbers"] and [AgentX "Serving numbers"]: 8K-token
+ * prefill chunks over long cached prefixes).  Each sequence b appends a chunk
+ * of n_b = query_start_loc[b+1] - query_start_loc[b] tokens whose KV is stored
+ * first (chunk_latent/chunk_rope/chunk_idx_k/chunk_idx_scale at slot_mapping,
+ * required); seq_lens[b] includes the chunk, and chunk token i attends the
+ * positions <= seq_lens[b] - n_b + i (causal within the chunk, the whole
+ * prefix before it).
+ *   chunk_len: the largest n_b of the call (the query-group bound of the
+ *     indexer); other arguments and results as smla_decode.
+ *   Returns SMLA_ERR_INVALID_ARG when slot_mapping or a chunk input is NULL.
+ */
+smla_status_t smla_prefill_chunk(const smla_layout_t* layout, const smla_params_t* params, void* pool,
+                                 int layer, const void* chunk_latent, const void* chunk_rope,
+                                 const uint8_t* chunk_idx_k, const float* chunk_idx_scale,
+                                 const int64_t* slot_mapping, const void* q, const void* q_pe,
+                                 const uint8_t* q_idx, const float* w, const int32_t* block_table,
+                                 int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
+                                 int batch, int n_tokens, int chunk_len, int max_ctx, void* out, float* lse,
+                                 int32_t* topk_idx_out, void* workspace, size_t workspace_bytes,
+                                 void* stream);
+
+/*
  * smla_decode_static -- smla_decode for callers that cannot allocate device
  * memory, such as code whose device memory is entirely owned by a serving
  * engine's allocator (one that reserves all free HBM for the KV block pool and

@@ -17,13 +17,13 @@ from . import build_lib
 __all__ = [
     "SmlaError", "Layout", "Params", "lib", "layout_init", "workspace_size", "kvpack_store",
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
-    "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static",
+    "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static", "smla_prefill_chunk",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
-    "smla_decode_static",
+    "smla_decode_static", "smla_prefill_chunk",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
@@ -83,6 +83,8 @@ def lib() -> ctypes.CDLL:
                                  _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "smla_decode_static": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
                                         _I, _I, _I, _P, _P, _P, _P]),
+            "smla_prefill_chunk": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
+                                        _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "smla_get_last_error": (_I, [_P]),
             "smla_status_string": (ctypes.c_char_p, [_I]),
             "smla_version": (_I, []),
@@ -217,6 +219,21 @@ def smla_decode_static(layout, params, pool, layer, new_latent, new_rope, new_id
                                     _ptr(seq_lens), _ptr(query_start_loc), seq_lens.numel(), q.shape[0], max_q,
                                     max_ctx, _ptr(out), _ptr(lse), _ptr(topk_idx_out), _stream(stream)),
            "smla_decode_static")
+
+
+def smla_prefill_chunk(layout, params, pool, layer, chunk_latent, chunk_rope, chunk_idx_k, chunk_idx_scale,
+                       slot_mapping, q, q_pe, q_idx, w, block_table, seq_lens, query_start_loc, chunk_len, max_ctx,
+                       out, lse, workspace, topk_idx_out=None, stream=None):
+    """A prefill chunk per sequence (its keys stored first), causal within the chunk."""
+    _expect(q, torch.bfloat16, "q")
+    _expect(workspace, torch.uint8, "workspace")
+    _expect(slot_mapping, torch.int64, "slot_mapping")
+    _check(lib().smla_prefill_chunk(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(chunk_latent),
+                                    _ptr(chunk_rope), _ptr(chunk_idx_k), _ptr(chunk_idx_scale), _ptr(slot_mapping),
+                                    _ptr(q), _ptr(q_pe), _ptr(q_idx), _ptr(w), _ptr(block_table), block_table.shape[1],
+                                    _ptr(seq_lens), _ptr(query_start_loc), seq_lens.numel(), q.shape[0], chunk_len,
+                                    max_ctx, _ptr(out), _ptr(lse), _ptr(topk_idx_out), _ptr(workspace),
+                                    workspace.numel(), _stream(stream)), "smla_prefill_chunk")
 
 
 def smla_get_last_error(stream=None) -> int:

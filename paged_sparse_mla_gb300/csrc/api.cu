@@ -243,6 +243,22 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
   return SMLA_OK;
 }
 
+smla_status_t smla_prefill_chunk(const smla_layout_t* layout, const smla_params_t* params, void* pool, int layer,
+                                 const void* chunk_latent, const void* chunk_rope, const uint8_t* chunk_idx_k,
+                                 const float* chunk_idx_scale, const int64_t* slot_mapping, const void* q,
+                                 const void* q_pe, const uint8_t* q_idx, const float* w, const int32_t* block_table,
+                                 int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc, int batch,
+                                 int n_tokens, int chunk_len, int max_ctx, void* out, float* lse,
+                                 int32_t* topk_idx_out, void* workspace, size_t workspace_bytes, void* stream) {
+  // The chunk's own keys must be in the pool before any of its tokens is scored.
+  if (n_tokens > 0 && (slot_mapping == nullptr || chunk_latent == nullptr || chunk_idx_k == nullptr ||
+                       chunk_idx_scale == nullptr || (layout != nullptr && layout->d_rope > 0 && chunk_rope == nullptr)))
+    return SMLA_ERR_INVALID_ARG;
+  return smla_decode(layout, params, pool, layer, chunk_latent, chunk_rope, chunk_idx_k, chunk_idx_scale, slot_mapping,
+                     q, q_pe, q_idx, w, block_table, bt_stride, seq_lens, query_start_loc, batch, n_tokens, chunk_len,
+                     max_ctx, out, lse, topk_idx_out, workspace, workspace_bytes, stream);
+}
+
 smla_status_t smla_get_last_error(void* stream) {
   DeviceInfo* d = current_device();
   if (d == nullptr) return SMLA_ERR_CUDA;

@@ -64,6 +64,11 @@ def test_host_side_argument_checks(lib):
     assert lib.smla_attend(L, P, None, 0, None, None, None, None, 0, None, 1, 3, None, None, None) == 1
     assert lib.smla_decode(L, P, None, 0, None, None, None, None, None, None, None, None, None, None, 0, None,
                            None, 1, 4, 1, 100, None, None, None, None, 0, None) == 1
+    # prefill chunks must store their own keys first: no slot mapping is an argument error
+    assert lib.smla_prefill_chunk(L, P, None, 0, None, None, None, None, None, None, None, None, None, None, 0, None,
+                                  None, 1, 4, 4, 100, None, None, None, None, 0, None) == 1
+    assert lib.smla_prefill_chunk(L, P, None, 0, None, None, None, None, None, None, None, None, None, None, 0, None,
+                                  None, 1, 0, 4, 100, None, None, None, None, 0, None) == 0  # an empty chunk
     assert lib.smla_workspace_size(L, P, 0, 100) == 0
     assert lib.smla_workspace_size(L, P, 4, 1000) >= 4 * 1000 * 4 + 4 * 2048 * 4
     assert lib.smla_status_string(4) == b"SMLA_ERR_BAD_INDEX"

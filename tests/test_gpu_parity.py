@@ -9,6 +9,7 @@ import pytest
 import torch
 
 import oracle
+import paged_sparse_mla_gb300 as smla
 from paged_sparse_mla_gb300.workloads import FULL, TINY, build_workload, make_config
 from tests.oracle_helpers import bits, layout_of, npy, oracle_pool, oracle_step, sequence_slots
 from tests import gpu_helpers as G
@@ -78,6 +79,31 @@ def test_fused_decode_equals_stages(name):
     assert a["err"] == 0 and b["err"] == 0
     assert np.array_equal(a["topk"], b["topk"])
     assert np.array_equal(a["out"], b["out"]) and np.array_equal(a["lse"], b["lse"])
+
+
+def test_prefill_chunk_matches_oracle_and_decode():
+    """smla_prefill_chunk: a causal chunk on a cached prefix, checked against the oracle and smla_decode."""
+    wl = CASES["prefill-scaled"]()
+    ref_pool = oracle_pool(wl)
+    ref = oracle_step(wl, ref_pool)
+    g = G.cuda_wl(CASES["prefill-scaled"]())
+    lay, prm = G.gpu_layout(g), G.gpu_params(g)
+    pool = G.gpu_pool(g, lay)
+    d = g.dims
+    T = g.n_tokens
+    ws = torch.empty(smla.workspace_size(lay, prm, T, g.max_ctx), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
+    topk = torch.empty((T, prm.top_k), dtype=torch.int32, device="cuda")
+    smla.smla_prefill_chunk(lay, prm, pool, 0, g.new_latent, g.new_rope, g.new_idx_k, g.new_idx_s, g.slot_mapping, g.q,
+                            g.q_pe, g.q_idx, g.w, g.block_table, g.seq_lens, g.query_start_loc, g.max_q, g.max_ctx,
+                            out, lse, ws, topk_idx_out=topk)
+    assert smla.smla_get_last_error() == 0
+    assert np.array_equal(pool.cpu().numpy(), ref_pool)
+    res = dict(topk=topk.cpu().numpy(), out=out.float().cpu().numpy(), lse=lse.cpu().numpy())
+    _compare_all(wl, res, ref, "prefill_chunk")
+    b = G.run_decode(g, G.gpu_pool(g, lay), lay, prm)
+    assert np.array_equal(res["topk"], b["topk"]) and np.array_equal(res["out"], b["out"])
 
 
 def test_sparse_equals_dense_when_topk_covers_context():
