@@ -25,6 +25,9 @@ Sources, abbreviated in the docstrings below:
   prompts inside the top-k still take the sparse MQA kernel; FP8 KV cache).
 * [OCP-FP8] -- the OCP 8-bit floating point specification (E4M3 format).
 
+``oracle.dcp`` states the split-context form (token shards, candidate merge,
+log-sum-exp merge of partial outputs) of [AgentX "Kimi K3"] DCP.
+
 The pages give no formulas.  Where a step is not fixed by them, the reading
 taken here is the plainest one consistent with the rest (score function
 sum_h w_h * ReLU(q_h . k) * s_k, per-tile amax/448 quantisation, ties to the
@@ -42,10 +45,11 @@ from .topk import topk_select
 from .attention import attend, sparse_attend, dense_attend
 from .pipeline import decode_step
 from .store import bf16_bits_to_f64, quantize_latent
+from . import dcp
 
 __all__ = [
     "e4m3_decode", "e4m3_encode", "E4M3_MAX", "PoolLayout", "kvpack_store",
     "read_record", "read_index_key", "index_scores", "index_scores_row",
     "query_positions", "context_slots", "topk_select", "attend", "sparse_attend",
-    "dense_attend", "decode_step", "bf16_bits_to_f64", "quantize_latent",
+    "dense_attend", "decode_step", "bf16_bits_to_f64", "quantize_latent", "dcp",
 ]

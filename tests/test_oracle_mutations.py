@@ -15,6 +15,8 @@ import oracle.pipeline
 from tests import test_oracle_attention as ta
 from tests import test_oracle_indexer_topk as ti
 from tests import test_oracle_layout_store as ts
+from tests import test_oracle_dcp as td
+import oracle.dcp
 
 
 def _attend_no_rope(q, q_pe, lat, rope, sigma):
@@ -49,7 +51,43 @@ def _scores_no_relu(layout, pool, layer, q_codes, w, bt_row, p, chunk=1 << 17):
 
 
 
+_orig_lse_merge = oracle.dcp.lse_merge
+_orig_topk_merge = oracle.dcp.topk_merge
+
+
+def _lse_merge_unweighted(parts_out, parts_lse):
+    out, lse = _orig_lse_merge(parts_out, parts_lse)
+    return np.asarray(parts_out, np.float64).mean(axis=0), lse
+
+
+def _lse_merge_max_only(parts_out, parts_lse):
+    out, _ = _orig_lse_merge(parts_out, parts_lse)
+    return out, np.asarray(parts_lse, np.float64).max(axis=0)
+
+
+def _topk_merge_local_order(shard_scores, shard_topk, n_shards, k):
+    # mistake: ties broken by shard first, then local position, instead of by global position
+    glob, per = _orig_topk_merge(shard_scores, shard_topk, n_shards, k)
+    cand = []
+    for r in range(n_shards):
+        loc = np.asarray(shard_topk[r], np.int64)
+        loc = loc[loc >= 0]
+        for i in loc:
+            cand.append((-float(np.asarray(shard_scores[r], np.float32)[i]), r, int(i), int(i) * n_shards + r))
+    cand.sort()
+    keep = np.sort(np.array([c[3] for c in cand[:k]], dtype=np.int64))
+    g = np.full(k, -1, dtype=np.int32)
+    g[:keep.size] = keep
+    return g, per
+
+
 CASES = [
+    ("merge without lse weights", oracle.dcp, "lse_merge", _lse_merge_unweighted,
+     lambda: td.test_lse_merge_equals_attention_over_all_keys(3)),
+    ("merged lse as the max", oracle.dcp, "lse_merge", _lse_merge_max_only,
+     lambda: td.test_lse_merge_identity_and_empty_parts()),
+    ("candidate ties by shard", oracle.dcp, "topk_merge", _topk_merge_local_order,
+     lambda: td.test_topk_merge_equals_unsharded_topk(3, 300, 64)),
     ("attention drops rope", oracle.attention, "attend", _attend_no_rope,
      lambda: ta.test_attend_matches_torch_sdpa(64)),
     ("lse in log2", oracle.attention, "attend", _attend_lse_log2,
@@ -64,7 +102,7 @@ CASES = [
 @pytest.mark.parametrize("name,mod,attr,bad,pin", CASES, ids=[c[0] for c in CASES])
 def test_pin_catches_planted_mistake(monkeypatch, name, mod, attr, bad, pin):
     monkeypatch.setattr(mod, attr, bad)
-    for m in (oracle, oracle.pipeline, ta, ti):
+    for m in (oracle, oracle.pipeline, ta, ti, td.dcp):
         if hasattr(m, attr):
             monkeypatch.setattr(m, attr, bad, raising=False)
     with pytest.raises(AssertionError):
