@@ -256,6 +256,45 @@ smla_status_t smla_decode_static(const smla_layout_t* layout, const smla_params_
                                  int batch, int n_tokens, int max_q, int max_ctx, void* out, float* lse,
                                  int32_t* topk_idx_out, void* stream);
 
+/*
+ * Split-context (DCP-style) decode, emulated with N token shards on one GPU
+ * ([AgentX "Kimi K3"]: decode context parallelism with an LSE merge of partial
+ * outputs; [GLM-5.3 "What is new"]: DCP8 decode).  Shard r holds the positions
+ * j = N*i + r of every sequence at local position i; each shard runs
+ * smla_index_scores and smla_topk over its own positions (a query at global
+ * position p sees local positions 0 .. (p - r) / N), then:
+ *
+ * smla_dcp_topk_merge -- the candidate exchange.  For every query token t the
+ * union of the shards' local top-k candidates (score, global position) is
+ * reduced to the top_k highest by (score desc, global position asc), which is
+ * the unsharded selection; shard r receives its selected local positions.
+ *   shard_scores: fp32, shard r's score row of token t at
+ *     shard_scores[r * shard_stride + t * row_stride + i] (i = local position)
+ *   shard_topk: int32 [n_shards, n_tokens, top_k], each row ascending, -1 padded
+ *     (smla_topk's output on each shard)
+ *   shard_sel: int32 [n_shards, n_tokens, top_k] out, selected local positions
+ *     ascending, -1 padded (the top-k input of smla_attend on shard r)
+ *   merged: optional int32 [n_tokens, top_k] out, the selected global positions
+ *     ascending, -1 padded (NULL = not written)
+ *   n_shards * top_k <= 16384 and top_k <= 4096, else SMLA_ERR_UNSUPPORTED.
+ */
+smla_status_t smla_dcp_topk_merge(const float* shard_scores, int64_t shard_stride, int64_t row_stride,
+                                  const int32_t* shard_topk, int n_shards, int n_tokens, int top_k,
+                                  int32_t* shard_sel, int32_t* merged, void* stream);
+
+/*
+ * smla_lse_merge -- the output exchange: combine the shards' partial results
+ * (smla_attend on each shard over its shard_sel) into
+ *   lse = ln sum_r exp(lse_r),  out = sum_r exp(lse_r - lse) * out_r
+ * in fp32 (a shard with lse_r = -inf contributes nothing; all -inf gives out = 0,
+ * lse = -inf).
+ *   parts_out: bf16 [n_shards, n_tokens, n_heads, d], 16-byte aligned, d % 8 == 0
+ *   parts_lse: fp32 [n_shards, n_tokens, n_heads]
+ *   out: bf16 [n_tokens, n_heads, d] (16-byte aligned), lse: fp32 [n_tokens, n_heads]
+ */
+smla_status_t smla_lse_merge(const void* parts_out, const float* parts_lse, int n_shards, int n_tokens,
+                             int n_heads, int d, void* out, float* lse, void* stream);
+
 /* Synchronise `stream`, return the latched device error (and clear it). */
 smla_status_t smla_get_last_error(void* stream);
 

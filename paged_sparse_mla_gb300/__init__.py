@@ -18,12 +18,13 @@ __all__ = [
     "SmlaError", "Layout", "Params", "lib", "layout_init", "workspace_size", "kvpack_store",
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
     "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static", "smla_prefill_chunk",
+    "smla_dcp_topk_merge", "smla_lse_merge",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
-    "smla_decode_static", "smla_prefill_chunk",
+    "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
@@ -85,6 +86,8 @@ def lib() -> ctypes.CDLL:
                                         _I, _I, _I, _P, _P, _P, _P]),
             "smla_prefill_chunk": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
                                         _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
+            "smla_dcp_topk_merge": (_I, [_P, _I64, _I64, _P, _I, _I, _I, _P, _P, _P]),
+            "smla_lse_merge": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
             "smla_get_last_error": (_I, [_P]),
             "smla_status_string": (ctypes.c_char_p, [_I]),
             "smla_version": (_I, []),
@@ -234,6 +237,28 @@ def smla_prefill_chunk(layout, params, pool, layer, chunk_latent, chunk_rope, ch
                                     _ptr(seq_lens), _ptr(query_start_loc), seq_lens.numel(), q.shape[0], chunk_len,
                                     max_ctx, _ptr(out), _ptr(lse), _ptr(topk_idx_out), _ptr(workspace),
                                     workspace.numel(), _stream(stream)), "smla_prefill_chunk")
+
+
+def smla_dcp_topk_merge(shard_scores, shard_topk, shard_sel, merged=None, stream=None):
+    """Candidate merge over token shards.  shard_scores [N, T, stride] fp32, shard_topk / shard_sel [N, T, k] int32."""
+    _expect(shard_scores, torch.float32, "shard_scores")
+    _expect(shard_topk, torch.int32, "shard_topk")
+    _expect(shard_sel, torch.int32, "shard_sel")
+    n, t, k = shard_topk.shape
+    _check(lib().smla_dcp_topk_merge(_ptr(shard_scores), shard_scores.stride(0), shard_scores.stride(1),
+                                     _ptr(shard_topk), n, t, k, _ptr(shard_sel), _ptr(merged), _stream(stream)),
+           "smla_dcp_topk_merge")
+
+
+def smla_lse_merge(parts_out, parts_lse, out, lse, stream=None):
+    """LSE merge of partial outputs.  parts_out [N, T, H, D] bf16, parts_lse [N, T, H] fp32."""
+    _expect(parts_out, torch.bfloat16, "parts_out")
+    _expect(parts_lse, torch.float32, "parts_lse")
+    _expect(out, torch.bfloat16, "out")
+    _expect(lse, torch.float32, "lse")
+    n, t, h, d = parts_out.shape
+    _check(lib().smla_lse_merge(_ptr(parts_out), _ptr(parts_lse), n, t, h, d, _ptr(out), _ptr(lse), _stream(stream)),
+           "smla_lse_merge")
 
 
 def smla_get_last_error(stream=None) -> int:

@@ -247,3 +247,61 @@ def make_config(i: int, device="cpu", *, scale: float = 1.0) -> Workload:
         return build_workload("prefill-131k+8k", FULL, [prefix + chunk], [chunk], seed=4,
                               device=device, slack_blocks=64)
     raise ValueError(f"unknown config {i}")
+
+
+# ----------------------------------------------------------------------------- token shards
+def shard_visible(p: int, r: int, n_shards: int) -> int:
+    """Local positions of shard r (global positions r, r + N, ...) visible from global position p."""
+    return 0 if p < r else (p - r) // n_shards + 1
+
+
+def shard_pools(wl: Workload, layout, pool: torch.Tensor, n_shards: int, *, seed: int, layer: int = 0):
+    """Split a decode workload's context into N round-robin token shards, each in its own pool.
+
+    Global position j of sequence b goes to shard r = j % N at local position
+    j // N, in a fresh pool with its own (randomly permuted) block table; the
+    record, indexer key and indexer scale bytes of each position are copied from
+    ``pool`` (which must already hold every position, this step's included).
+    One query token per sequence (at position seq_len - 1) is assumed.
+    Returns, per shard, dict(layout, pool, block_table, seq_lens, max_ctx).
+    """
+    from . import layout_init  # the package's C-ABI binding
+
+    d = wl.dims
+    bs = d.block_size
+    dev = pool.device
+    rng = np.random.default_rng(seed)
+    bt = wl.block_table.cpu().numpy()
+    lens = wl.seq_lens.cpu().numpy()
+    shards = []
+    for r in range(n_shards):
+        lr = [shard_visible(int(n) - 1, r, n_shards) for n in lens]
+        nblk = [(x + bs - 1) // bs for x in lr]
+        total = sum(nblk) + 1
+        lay_r = layout_init(bs, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, total)
+        pool_r = torch.zeros(lay_r.pool_bytes, dtype=torch.uint8, device=dev)
+        perm = rng.permutation(total)
+        bt_r = np.zeros((len(lens), max(1, max(nblk))), dtype=np.int32)
+        nxt = 0
+        src, dst = [], []
+        for b in range(len(lens)):
+            bt_r[b, :nblk[b]] = perm[nxt:nxt + nblk[b]]
+            nxt += nblk[b]
+            i = np.arange(lr[b], dtype=np.int64)
+            j = i * n_shards + r
+            src.append(bt[b, j // bs].astype(np.int64) * bs + j % bs)
+            dst.append(bt_r[b, i // bs].astype(np.int64) * bs + i % bs)
+        src = torch.as_tensor(np.concatenate(src), device=dev)
+        dst = torch.as_tensor(np.concatenate(dst), device=dev)
+        if src.numel():
+            for name, unit in (("rec_off", layout.rec_stride), ("idx_key_off", layout.d_index), ("idx_scale_off", 4)):
+                ar = torch.arange(unit, device=dev, dtype=torch.int64)
+                s0 = (src // bs) * layout.block_stride + layer * layout.layer_stride + getattr(layout, name) + \
+                    (src % bs) * unit
+                d0 = (dst // bs) * lay_r.block_stride + layer * lay_r.layer_stride + getattr(lay_r, name) + \
+                    (dst % bs) * unit
+                pool_r[(d0[:, None] + ar).reshape(-1)] = pool[(s0[:, None] + ar).reshape(-1)]
+        shards.append(dict(layout=lay_r, pool=pool_r, block_table=torch.as_tensor(bt_r, device=dev),
+                           seq_lens=torch.as_tensor(np.asarray(lr, dtype=np.int32), device=dev),
+                           max_ctx=max(1, max(lr))))
+    return shards

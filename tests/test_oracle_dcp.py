@@ -108,3 +108,12 @@ def test_sharded_sparse_attention_equals_unsharded(n_shards):
     out, lse = dcp.lse_merge(np.stack(outs), np.stack(lses))
     assert np.array_equal(np.sort(glob[glob >= 0]), np.sort(sel))
     assert np.allclose(out, out_ref, rtol=0, atol=1e-12) and np.allclose(lse, lse_ref, rtol=0, atol=1e-12)
+
+
+def test_workload_shard_rule_matches_oracle():
+    """The workload builder's shard visibility (used to build GPU shard pools) follows the oracle's rule."""
+    from paged_sparse_mla_gb300 import workloads
+    for n_shards in (1, 2, 3, 8):
+        for p in range(50):
+            for r in range(n_shards):
+                assert workloads.shard_visible(p, r, n_shards) == dcp.shard_visible(p, r, n_shards)
