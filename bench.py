@@ -490,6 +490,129 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------------------- split-context (DCP) arm
+def run_dcp(args):
+    """--dcp N: the decode step split over N round-robin token shards on one GPU.
+
+    A step = per shard (indexer scores, top-k) -> smla_dcp_topk_merge -> per shard
+    attention -> smla_lse_merge, over every query token of a decode workload
+    (one query token per sequence).  Prints one JSON line with tokens/s, the
+    per-phase device times, the unsharded fused step on the same inputs for
+    context, and the merge kernel's roofline.
+    """
+    import paged_sparse_mla_gb300 as smla
+    from paged_sparse_mla_gb300 import build_lib
+    from paged_sparse_mla_gb300.workloads import make_config, shard_pools
+
+    torch.cuda.set_device(0)
+    build_lib.build()
+    smla.lib()
+    n_sh = args.dcp
+    wl = make_config(args.workload, device="cuda", scale=args.scale)
+    if wl.max_q != 1:
+        raise SystemExit("--dcp needs a decode workload with one query token per sequence (workloads 2 and 4)")
+    d = wl.dims
+    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
+    pool = torch.zeros(lay.pool_bytes, dtype=torch.uint8, device="cuda")
+    s = wl.cached_slots
+    for c0 in range(0, s.numel(), 1 << 20):
+        sl = s[c0:c0 + (1 << 20)].contiguous()
+        smla.kvpack_store(lay, pool, 0, wl.slot_latent[sl].contiguous(), wl.slot_rope[sl].contiguous(),
+                          wl.slot_idx_k[sl].contiguous(), wl.slot_idx_s[sl].contiguous(), sl)
+    smla.kvpack_store(lay, pool, 0, wl.new_latent, wl.new_rope, wl.new_idx_k, wl.new_idx_s, wl.slot_mapping)
+    wl.slot_latent = wl.slot_rope = wl.slot_idx_k = wl.slot_idx_s = None
+    shards = shard_pools(wl, lay, pool, n_sh, seed=17)
+    torch.cuda.empty_cache()
+    T, k = wl.n_tokens, d.top_k
+    stride = max((x["max_ctx"] + 3) // 4 * 4 for x in shards)
+    scores = torch.empty((n_sh, T, stride), dtype=torch.float32, device="cuda")
+    topk = torch.empty((n_sh, T, k), dtype=torch.int32, device="cuda")
+    sel = torch.empty((n_sh, T, k), dtype=torch.int32, device="cuda")
+    parts = torch.empty((n_sh, T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    parts_lse = torch.empty((n_sh, T, d.n_heads), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
+    stream = torch.cuda.current_stream()
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def phase_local():
+        for r, x in enumerate(shards):
+            smla.smla_index_scores(x["layout"], prm, x["pool"], 0, wl.q_idx, wl.w, x["block_table"], x["seq_lens"],
+                                   wl.query_start_loc, 1, x["max_ctx"], scores[r], stream=stream)
+            smla.smla_topk(prm, scores[r], x["seq_lens"], wl.query_start_loc, topk[r], stream=stream)
+
+    def phase_merge():
+        smla.smla_dcp_topk_merge(scores, topk, sel, stream=stream)
+
+    def phase_attend():
+        for r, x in enumerate(shards):
+            smla.smla_attend(x["layout"], prm, x["pool"], 0, wl.q, wl.q_pe, sel[r], x["block_table"],
+                             wl.query_start_loc, parts[r], parts_lse[r], stream=stream)
+
+    def phase_lse():
+        smla.smla_lse_merge(parts, parts_lse, out, lse, stream=stream)
+
+    phases = [("local index+topk", phase_local), ("topk merge", phase_merge), ("attention", phase_attend),
+              ("lse merge", phase_lse)]
+    for _ in range(args.warmup):
+        for _, f in phases:
+            f()
+    torch.cuda.synchronize()
+    if smla.smla_get_last_error() != 0:
+        raise RuntimeError("device error during warm-up")
+    clocks = ClockSampler(0)
+    time.sleep(0.3)
+    torch.cuda._sleep(4_000_000)
+    marks = [[ev() for _ in range(len(phases) + 1)] for _ in range(args.steps)]
+    for st in range(args.steps):
+        marks[st][0].record(stream)
+        for i, (_, f) in enumerate(phases):
+            f()
+            marks[st][i + 1].record(stream)
+    torch.cuda.synchronize()
+    clk = clocks.stop()
+    if smla.smla_get_last_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    ms_total = sum(marks[st][0].elapsed_time(marks[st][-1]) for st in range(args.steps))
+    ph_ms = {name: statistics.median(marks[st][i].elapsed_time(marks[st][i + 1]) for st in range(args.steps))
+             for i, (name, _) in enumerate(phases)}
+    value = whole_job_rate(T, 1, args.steps, ms_total)
+    # the unsharded fused step on the same inputs (context)
+    ws = torch.empty(smla.workspace_size(lay, prm, T, wl.max_ctx), dtype=torch.uint8, device="cuda")
+    o2 = torch.empty_like(out)
+    l2 = torch.empty_like(lse)
+    for _ in range(2):
+        smla.smla_decode(lay, prm, pool, 0, None, None, None, None, None, wl.q, wl.q_pe, wl.q_idx, wl.w,
+                         wl.block_table, wl.seq_lens, wl.query_start_loc, 1, wl.max_ctx, o2, l2, ws, stream=stream)
+    a, b = ev(), ev()
+    a.record(stream)
+    for _ in range(args.steps):
+        smla.smla_decode(lay, prm, pool, 0, None, None, None, None, None, wl.q, wl.q_pe, wl.q_idx, wl.w,
+                         wl.block_table, wl.seq_lens, wl.query_start_loc, 1, wl.max_ctx, o2, l2, ws, stream=stream)
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms_whole = a.elapsed_time(b) / args.steps
+    pk = peaks()
+    lse_bytes = n_sh * T * d.n_heads * (2 * d.d_latent + 4) + T * d.n_heads * (2 * d.d_latent + 4)
+    ach = lse_bytes / (ph_ms["lse merge"] / 1e3) / 1e9
+    line = {
+        "metric": f"split-context sparse-MLA decode tokens/s, {n_sh} round-robin token shards on one GPU",
+        "value": round(value, 1), "unit": UNIT, "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3+bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": wl.name, "shards": n_sh, "batch": int(wl.seq_lens.numel()), "query_tokens": T,
+                   "max_ctx": int(wl.max_ctx), "top_k": k, "l2": "inputs larger than L2"},
+        "phases_ms": {k2: round(v, 4) for k2, v in ph_ms.items()},
+        "unsharded_fused_ms": round(ms_whole, 4),
+        "roofline": {"kernel": "smla_lse_merge", "bound": "hbm", "achieved": round(ach, 1), "peak": pk["hbm"],
+                     "unit": "GB/s", "frac": round(ach / pk["hbm"], 4), "traffic": None,
+                     "alg_bytes_per_launch": lse_bytes},
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -499,6 +622,8 @@ def main():
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--dcp", type=int, default=0,
+                    help="split-context arm: N round-robin token shards on one GPU (decode workloads 2 and 4)")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="shrink context lengths (profiler captures of a smaller case; not a bench line)")
     args = ap.parse_args()
@@ -506,6 +631,8 @@ def main():
         args.warmup = 3
     if args.impl == "reference":
         run_reference(args)
+    elif args.dcp > 0:
+        run_dcp(args)
     else:
         run_gpu(args)
 

@@ -11,8 +11,10 @@
 //     candidates is reduced to the k highest by (score desc, position asc) --
 //     the unsharded selection -- and each shard receives its selected local
 //     positions in ascending order (one CTA per query token; the candidates are
-//     sorted in shared memory as 64-bit (order-preserving score key, ~position)
-//     words, so every candidate is distinct and the k-th word is the cut);
+//     64-bit (order-preserving score key, ~position) words in shared memory, so
+//     every candidate is distinct; a radix select finds the k-th word, each
+//     shard's kept positions are compacted in list order, and the merged
+//     positions are placed by rank);
 //   * smla_lse_merge: out = sum_r exp(lse_r - lse) out_r, lse = ln sum_r
 //     exp(lse_r), fp32 arithmetic, bf16 out (one warp per query head, 16-byte
 //     loads and stores).
@@ -23,110 +25,190 @@ namespace {
 
 constexpr int kMergeThreads = 512;
 constexpr int kMaxCand = 16384;  // shards x top_k handled by one CTA
-constexpr int kMaxMergeK = 4096; // top_k of the merge (the merged-position sort buffer)
 
 __device__ __forceinline__ uint32_t order_key32(float x) {
   const uint32_t u = __float_as_uint(x + 0.0f);  // -0 -> +0
   return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// In-place bitonic sort, descending, of m (a power of two) 64-bit words in shared memory.
-__device__ void bitonic_desc(unsigned long long* a, int m) {
-  for (int size = 2; size <= m; size <<= 1) {
-    for (int stride = size >> 1; stride > 0; stride >>= 1) {
-      __syncthreads();
-      for (int i = threadIdx.x; i < m / 2; i += blockDim.x) {
-        const int lo = 2 * i - (i & (stride - 1));
-        const int hi = lo + stride;
-        const bool desc = (lo & size) == 0;
-        const unsigned long long x = a[lo], y = a[hi];
-        if (desc ? (x < y) : (x > y)) {
-          a[lo] = y;
-          a[hi] = x;
-        }
-      }
+// Exclusive prefix sum over the CTA (kMergeThreads threads); returns this thread's prefix and the total.
+__device__ __forceinline__ int cta_exclusive_scan(int v, int* warp_sums, int& total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) warp_sums[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < kMergeThreads / 32 ? warp_sums[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
     }
+    if (lane < kMergeThreads / 32) warp_sums[lane] = w;
   }
   __syncthreads();
+  total = warp_sums[kMergeThreads / 32 - 1];
+  const int before = warp > 0 ? warp_sums[warp - 1] : 0;
+  __syncthreads();
+  return before + x - v;
 }
+
+struct MergeSmem {
+  unsigned long long word[kMaxCand];  // candidate c = r * k + i, in the shards' list order
+  int sel[kMaxCand];                  // shard r's kept local positions at [r * k ...]
+  int hist[256];
+  int warp_sums[32];
+  int kept[64];                       // kept count per shard
+  unsigned long long prefix;
+  int remaining;
+};
 
 __global__ void __launch_bounds__(kMergeThreads) topk_merge_kernel(const float* __restrict__ scores, int64_t shard_stride,
                                                                  int64_t row_stride, const int32_t* __restrict__ topk,
                                                                  int n_shards, int n_tokens, int k,
                                                                  int32_t* __restrict__ shard_sel,
                                                                  int32_t* __restrict__ merged) {
-  extern __shared__ unsigned long long cand[];  // [m] sort buffer, then [k] merged positions (as words)
-  __shared__ unsigned long long cut;
-  __shared__ int n_valid;
+  extern __shared__ __align__(16) uint8_t merge_smem_raw[];
+  MergeSmem& sm = *reinterpret_cast<MergeSmem*>(merge_smem_raw);
   const int t = blockIdx.x;
   const int total = n_shards * k;
-  int m = 1;
-  while (m < total) m <<= 1;
-  if (threadIdx.x == 0) n_valid = 0;
-  __syncthreads();
-  // candidate (r, i) -> (key << 32) | ~j with j = loc * n_shards + r; empty slots are 0 (below any key)
-  int local_valid = 0;
-  for (int c = threadIdx.x; c < m; c += blockDim.x) {
-    unsigned long long w = 0;
-    if (c < total) {
-      const int r = c / k, i = c % k;
-      const int loc = __ldg(topk + (static_cast<int64_t>(r) * n_tokens + t) * k + i);
-      if (loc >= 0) {
-        const float s = __ldg(scores + r * shard_stride + static_cast<int64_t>(t) * row_stride + loc);
-        const uint32_t j = static_cast<uint32_t>(loc) * static_cast<uint32_t>(n_shards) + static_cast<uint32_t>(r);
-        w = (static_cast<unsigned long long>(order_key32(s)) << 32) | static_cast<uint32_t>(~j);
-        ++local_valid;
+  // candidate (r, i) -> (key << 32) | ~j, j = loc * n_shards + r; empty slots are 0 (below any key).
+  // In rounds of 8 per thread: top-k entries first, then the scores they point at, so each
+  // thread's loads are in flight together.
+  constexpr int kRound = 8;
+  int nv = 0;
+  for (int c0 = 0; c0 < total; c0 += kRound * kMergeThreads) {
+    int loc[kRound];
+    float sv[kRound];
+#pragma unroll
+    for (int x = 0; x < kRound; ++x) {
+      const int c = c0 + threadIdx.x + x * kMergeThreads;
+      loc[x] = c < total ? __ldg(topk + (static_cast<int64_t>(c / k) * n_tokens + t) * k + c % k) : -1;
+    }
+#pragma unroll
+    for (int x = 0; x < kRound; ++x) {
+      const int c = c0 + threadIdx.x + x * kMergeThreads;
+      sv[x] = loc[x] >= 0 ? __ldg(scores + (c / k) * shard_stride + static_cast<int64_t>(t) * row_stride + loc[x])
+                          : 0.f;
+    }
+#pragma unroll
+    for (int x = 0; x < kRound; ++x) {
+      const int c = c0 + threadIdx.x + x * kMergeThreads;
+      if (c < total) {
+        unsigned long long w = 0;
+        if (loc[x] >= 0) {
+          const uint32_t j = static_cast<uint32_t>(loc[x]) * static_cast<uint32_t>(n_shards) +
+                             static_cast<uint32_t>(c / k);
+          w = (static_cast<unsigned long long>(order_key32(sv[x])) << 32) | static_cast<uint32_t>(~j);
+          ++nv;
+        }
+        sm.word[c] = w;
       }
     }
-    cand[c] = w;
   }
-  atomicAdd(&n_valid, local_valid);
-  __syncthreads();
-  const int nv = n_valid;
-  // the k-th largest word is the cut: a candidate is kept iff its word >= cut
-  unsigned long long* sorted = cand;
-  bitonic_desc(sorted, m);
-  if (threadIdx.x == 0) cut = nv >= k ? sorted[k - 1] : 1ull;
-  __syncthreads();
-  const unsigned long long c_word = cut;
-  const int kept = nv < k ? nv : k;
-  // merged global positions, ascending: the first `kept` words hold them; sort them by position
-  if (merged != nullptr) {
-    unsigned long long* pos = cand + m;  // [mk] scratch after the sort buffer
-    int mk = 1;
-    while (mk < k) mk <<= 1;
-    for (int i = threadIdx.x; i < mk; i += blockDim.x)
-      pos[i] = i < kept ? static_cast<unsigned long long>(~static_cast<uint32_t>(sorted[i] & 0xFFFFFFFFull)) : 0ull;
-    bitonic_desc(pos, mk);  // positions descending (padding zeros last); written back reversed
-    for (int i = threadIdx.x; i < k; i += blockDim.x)
-      merged[static_cast<int64_t>(t) * k + i] = i < kept ? static_cast<int32_t>(pos[kept - 1 - i]) : -1;
-  }
-  // each shard's kept local positions, in the order of its (ascending) top-k list
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int n_warps = blockDim.x >> 5;
-  for (int r = warp; r < n_shards; r += n_warps) {
-    const int32_t* row = topk + (static_cast<int64_t>(r) * n_tokens + t) * k;
-    const float* srow = scores + r * shard_stride + static_cast<int64_t>(t) * row_stride;
-    int32_t* out = shard_sel + (static_cast<int64_t>(r) * n_tokens + t) * k;
-    int written = 0;
-    for (int i0 = 0; i0 < k; i0 += 32) {
-      const int i = i0 + lane;
-      bool keep = false;
-      int loc = -1;
-      if (i < k) {
-        loc = __ldg(row + i);
-        if (loc >= 0) {
-          const uint32_t j = static_cast<uint32_t>(loc) * static_cast<uint32_t>(n_shards) + static_cast<uint32_t>(r);
-          const unsigned long long w =
-              (static_cast<unsigned long long>(order_key32(__ldg(srow + loc))) << 32) | static_cast<uint32_t>(~j);
-          keep = w >= c_word;
+  int n_valid;
+  cta_exclusive_scan(nv, sm.warp_sums, n_valid);
+  // the k-th largest word (all words distinct): radix select, 8 bits a pass from the top
+  unsigned long long cut = 1ull;  // fewer than k candidates: keep every valid one
+  if (n_valid > k) {
+    if (threadIdx.x == 0) {
+      sm.prefix = 0ull;
+      sm.remaining = k;
+    }
+    unsigned long long mask = 0ull;
+    for (int shift = 56; shift >= 0; shift -= 8) {
+      for (int i = threadIdx.x; i < 256; i += kMergeThreads) sm.hist[i] = 0;
+      __syncthreads();
+      const unsigned long long pre = sm.prefix;
+      for (int c = threadIdx.x; c < total; c += kMergeThreads) {
+        const unsigned long long w = sm.word[c];
+        if ((w & mask) == pre) atomicAdd(&sm.hist[(w >> shift) & 0xFF], 1);
+      }
+      __syncthreads();
+      if (threadIdx.x < 32) {  // highest bin whose suffix count reaches `remaining`
+        const int lane = threadIdx.x;
+        int cnt[8], sum = 0;
+#pragma unroll
+        for (int x = 0; x < 8; ++x) {
+          cnt[x] = sm.hist[255 - (lane * 8 + x)];
+          sum += cnt[x];
+        }
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const int y = __shfl_up_sync(0xffffffffu, incl, o);
+          if (lane >= o) incl += y;
+        }
+        const int need = sm.remaining;
+        int above = incl - sum;
+        const bool here = above < need && incl >= need;
+        if (here) {
+          for (int x = 0; x < 8; ++x) {
+            if (above + cnt[x] >= need) {
+              sm.prefix = pre | (static_cast<unsigned long long>(255 - (lane * 8 + x)) << shift);
+              sm.remaining = need - above;
+              break;
+            }
+            above += cnt[x];
+          }
         }
       }
-      const uint32_t mask = __ballot_sync(0xffffffffu, keep);
-      if (keep) out[written + __popc(mask & ((1u << lane) - 1u))] = loc;
-      written += __popc(mask);
+      mask |= 0xFFull << shift;
+      __syncthreads();
     }
-    for (int i = written + lane; i < k; i += 32) out[i] = -1;
+    cut = sm.prefix;  // every word is distinct, so exactly k words are >= the k-th one
+  }
+  // each shard's kept local positions in list order (ascending), compacted by a CTA scan
+  for (int r = 0; r < n_shards; ++r) {
+    int base = 0;
+    for (int i0 = 0; i0 < k; i0 += kMergeThreads) {
+      const int i = i0 + threadIdx.x;
+      const unsigned long long w = i < k ? sm.word[r * k + i] : 0ull;
+      const bool keep = i < k && w != 0ull && w >= cut;
+      int tot;
+      const int pos = cta_exclusive_scan(keep ? 1 : 0, sm.warp_sums, tot);
+      if (keep) sm.sel[r * k + base + pos] = static_cast<int>((~static_cast<uint32_t>(w & 0xFFFFFFFFull) -
+                                                                static_cast<uint32_t>(r)) /
+                                                               static_cast<uint32_t>(n_shards));
+      base += tot;
+    }
+    if (threadIdx.x == 0) sm.kept[r] = base;
+  }
+  __syncthreads();
+  for (int r = 0; r < n_shards; ++r) {
+    int32_t* out = shard_sel + (static_cast<int64_t>(r) * n_tokens + t) * k;
+    for (int i = threadIdx.x; i < k; i += kMergeThreads) out[i] = i < sm.kept[r] ? sm.sel[r * k + i] : -1;
+  }
+  // merged global positions, ascending: an element's rank is the number of kept positions
+  // below it in every shard (binary search in each shard's ascending list)
+  if (merged != nullptr) {
+    int n_kept = 0;
+    for (int r = 0; r < n_shards; ++r) n_kept += sm.kept[r];
+    int32_t* mrow = merged + static_cast<int64_t>(t) * k;
+    for (int c = threadIdx.x; c < total; c += kMergeThreads) {
+      const int r = c / k, i = c % k;
+      if (i >= sm.kept[r]) continue;
+      const long long j = static_cast<long long>(sm.sel[c]) * n_shards + r;
+      int rank = i;
+      for (int r2 = 0; r2 < n_shards; ++r2) {
+        if (r2 == r) continue;
+        // kept local positions l of shard r2 with l * N + r2 < j
+        int lo = 0, hi = sm.kept[r2];
+        const int* list = sm.sel + r2 * k;
+        while (lo < hi) {
+          const int mid = (lo + hi) >> 1;
+          if (static_cast<long long>(list[mid]) * n_shards + r2 < j) lo = mid + 1; else hi = mid;
+        }
+        rank += lo;
+      }
+      mrow[rank] = static_cast<int32_t>(j);
+    }
+    for (int i = n_kept + threadIdx.x; i < k; i += kMergeThreads) mrow[i] = -1;
   }
 }
 
@@ -180,16 +262,13 @@ smla_status_t smla_dcp_topk_merge(const float* shard_scores, int64_t shard_strid
   if (n_tokens == 0) return SMLA_OK;
   if (!shard_scores || !shard_topk || !shard_sel || row_stride <= 0 || shard_stride < row_stride * n_tokens)
     return SMLA_ERR_INVALID_ARG;
-  if (static_cast<int64_t>(n_shards) * top_k > kMaxCand || top_k > kMaxMergeK) return SMLA_ERR_UNSUPPORTED;
-  int m = 1;
-  while (m < n_shards * top_k) m <<= 1;
-  int mk = 1;
-  while (mk < top_k) mk <<= 1;
-  const size_t smem = static_cast<size_t>(m + (merged ? mk : 0)) * sizeof(unsigned long long);
-  static bool attr_set = false;  // the largest dynamic size any call can ask for, set once
+  if (static_cast<int64_t>(n_shards) * top_k > kMaxCand) return SMLA_ERR_UNSUPPORTED;
+  if (n_shards > 64) return SMLA_ERR_UNSUPPORTED;
+  const size_t smem = sizeof(MergeSmem);
+  static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>((kMaxCand + kMaxMergeK) * sizeof(unsigned long long))) != cudaSuccess)
+    if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
       return SMLA_ERR_UNSUPPORTED;
     attr_set = true;
   }

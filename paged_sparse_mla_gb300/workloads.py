@@ -291,9 +291,10 @@ def shard_pools(wl: Workload, layout, pool: torch.Tensor, n_shards: int, *, seed
             j = i * n_shards + r
             src.append(bt[b, j // bs].astype(np.int64) * bs + j % bs)
             dst.append(bt_r[b, i // bs].astype(np.int64) * bs + i % bs)
-        src = torch.as_tensor(np.concatenate(src), device=dev)
-        dst = torch.as_tensor(np.concatenate(dst), device=dev)
-        if src.numel():
+        src_all = torch.as_tensor(np.concatenate(src), device=dev)
+        dst_all = torch.as_tensor(np.concatenate(dst), device=dev)
+        for c0 in range(0, src_all.numel(), 1 << 16):   # bounded index tensors
+            src, dst = src_all[c0:c0 + (1 << 16)], dst_all[c0:c0 + (1 << 16)]
             for name, unit in (("rec_off", layout.rec_stride), ("idx_key_off", layout.d_index), ("idx_scale_off", 4)):
                 ar = torch.arange(unit, device=dev, dtype=torch.int64)
                 s0 = (src // bs) * layout.block_stride + layer * layout.layer_stride + getattr(layout, name) + \
