@@ -10,8 +10,8 @@
 //   * 64 selected positions form a tile, and the tile buffer is double-buffered
 //     so that gathering tile t+1 overlaps the MMAs and the softmax of tile t.
 //     Eleven producer warps translate the logical positions through the block
-//     table two tiles ahead, read the 656-byte records (L2 prefetch with
-//     cp.async.bulk.prefetch), dequantise the E4M3 latent with its per-128 fp32
+//     table two tiles ahead, read the 656-byte records (one warp per record,
+//     two coalesced loads), dequantise the E4M3 latent with its per-128 fp32
 //     scales to bf16, and write the tile as 9 chunks of [64 keys x 64 dims] with
 //     the 128-byte swizzle (8 latent chunks + 1 rope chunk); the query is staged
 //     the same way (64 heads).
@@ -340,18 +340,15 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       constexpr int n_units = n_lat + kTile * 8;
       // Record addresses run two tiles ahead of the gather: during tile t, thread p < 64 reads
       // the top-k entry of key p of tile t+2 (before the gather), its block-table entry (after
-      // the first batch), and publishes the record address with an L2 prefetch (at the end).
+      // the first batch), and publishes the record address (at the end).
       const auto rec_of = [&](int j, int blk) -> const uint8_t* {
         if (j < 0) return nullptr;
         if (blk < 0 || blk >= L.num_blocks) {
           latch_error(A.err, SMLA_ERR_BAD_INDEX);
           return nullptr;
         }
-        const uint8_t* r = A.pool + static_cast<int64_t>(blk) * L.block_stride +
-                           static_cast<int64_t>(A.layer) * L.layer_stride + L.rec_off +
-                           static_cast<int64_t>(j % L.block_size) * L.rec_stride;
-        prefetch_l2_bulk(r, static_cast<uint32_t>(L.rec_stride));
-        return r;
+        return A.pool + static_cast<int64_t>(blk) * L.block_stride + static_cast<int64_t>(A.layer) * L.layer_stride +
+               L.rec_off + static_cast<int64_t>(j % L.block_size) * L.rec_stride;
       };
       const auto entry = [&](int tile) -> int {
         const int e = tile * kTile + ptid;
