@@ -613,6 +613,92 @@ def run_dcp(args):
     print(json.dumps(line))
 
 
+# ----------------------------------------------------------------------------- host-tier (HiSparse) arm
+def run_hisparse(args):
+    """--host-frac f: attention with the records of a fraction f of the blocks in pinned host memory.
+
+    The step's selection comes from one fused call; then smla_attend (every record in HBM) and
+    smla_attend_hisparse (records of the evicted blocks read from host memory over the CPU-GPU
+    link) are timed on the same selection.  Prints one JSON line.
+    """
+    import paged_sparse_mla_gb300 as smla
+    from paged_sparse_mla_gb300 import build_lib
+    from paged_sparse_mla_gb300.workloads import make_config, evict_records
+
+    torch.cuda.set_device(0)
+    build_lib.build()
+    smla.lib()
+    wl = make_config(args.workload, device="cuda", scale=args.scale)
+    d = wl.dims
+    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
+    pool = torch.zeros(lay.pool_bytes, dtype=torch.uint8, device="cuda")
+    s = wl.cached_slots
+    for c0 in range(0, s.numel(), 1 << 20):
+        sl = s[c0:c0 + (1 << 20)].contiguous()
+        smla.kvpack_store(lay, pool, 0, wl.slot_latent[sl].contiguous(), wl.slot_rope[sl].contiguous(),
+                          wl.slot_idx_k[sl].contiguous(), wl.slot_idx_s[sl].contiguous(), sl)
+    wl.slot_latent = wl.slot_rope = wl.slot_idx_k = wl.slot_idx_s = None
+    T = wl.n_tokens
+    ws = torch.empty(smla.workspace_size(lay, prm, T, wl.max_ctx), dtype=torch.uint8, device="cuda")
+    out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
+    topk = torch.empty((T, d.top_k), dtype=torch.int32, device="cuda")
+    smla.smla_decode(lay, prm, pool, 0, wl.new_latent, wl.new_rope, wl.new_idx_k, wl.new_idx_s, wl.slot_mapping,
+                     wl.q, wl.q_pe, wl.q_idx, wl.w, wl.block_table, wl.seq_lens, wl.query_start_loc, wl.max_q,
+                     wl.max_ctx, out, lse, ws, topk_idx_out=topk)
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream()
+
+    def timed(fn):
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(2_000_000)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    ms_hbm = timed(lambda: smla.smla_attend(lay, prm, pool, 0, wl.q, wl.q_pe, topk, wl.block_table,
+                                            wl.query_start_loc, out, lse, stream=stream))
+    bt = wl.block_table.cpu().numpy()
+    used = np.unique(bt[bt >= 0])
+    rng = np.random.default_rng(29)
+    moved = used[rng.random(used.size) < args.host_frac]
+    host, hmap = evict_records(lay, pool, moved)
+    clocks = ClockSampler(0)
+    time.sleep(0.3)
+    ms_tier = timed(lambda: smla.smla_attend_hisparse(lay, prm, pool, 0, host, hmap, wl.q, wl.q_pe, topk,
+                                                      wl.block_table, wl.query_start_loc, out, lse, stream=stream))
+    clk = clocks.stop()
+    if smla.smla_get_last_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    # records read from the host tier per step: selected positions whose block was evicted
+    tk = topk.cpu().numpy()
+    qsl = wl.query_start_loc.cpu().numpy()
+    seq = np.searchsorted(qsl, np.arange(T), side="right") - 1
+    blk = np.where(tk >= 0, bt[seq[:, None], np.maximum(tk, 0) // d.block_size], -1)
+    in_host = np.isin(blk, moved) & (tk >= 0)
+    host_bytes = int(in_host.sum()) * lay.rec_stride
+    line = {
+        "metric": "sparse-MLA attention tokens/s with part of the KV records in host memory (host-tier gather)",
+        "value": round(T / (ms_tier / 1e3), 1), "unit": UNIT, "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_tier, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "fp8e4m3+bf16 (fp32 accumulate)", "data": "synthetic",
+        "config": {"workload": wl.name, "host_fraction_of_blocks": args.host_frac, "blocks_moved": int(moved.size),
+                   "host_bytes_pinned": int(host.numel()), "query_tokens": T, "top_k": d.top_k},
+        "attend_all_hbm_ms": round(ms_hbm, 4),
+        "records_from_host_per_step": int(in_host.sum()), "host_bytes_per_step": host_bytes,
+        "host_read_gbs_if_overlapped": round(host_bytes / (ms_tier / 1e3) / 1e9, 1),
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -622,6 +708,8 @@ def main():
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--host-frac", type=float, default=0.0,
+                    help="host-tier arm: fraction of the blocks whose records live in pinned host memory")
     ap.add_argument("--dcp", type=int, default=0,
                     help="split-context arm: N round-robin token shards on one GPU (decode workloads 2 and 4)")
     ap.add_argument("--scale", type=float, default=1.0,
@@ -633,6 +721,8 @@ def main():
         run_reference(args)
     elif args.dcp > 0:
         run_dcp(args)
+    elif args.host_frac > 0:
+        run_hisparse(args)
     else:
         run_gpu(args)
 

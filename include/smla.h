@@ -181,6 +181,28 @@ smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* para
                           int batch, int n_tokens, void* out, float* lse, void* stream);
 
 /*
+ * smla_attend_hisparse -- smla_attend with a host tier for the selected
+ * records ([GLM-5.3 "What is new"]: Hybrid HiSparse decode keeps part of the
+ * KV in host memory and fetches the selected entries from there, so decode
+ * concurrency is no longer bounded by HBM).  The indexer keys stay in the HBM
+ * pool; the 656-byte records of evicted blocks live in a host buffer that the
+ * GPU reads directly (pinned, mapped host memory: on GB300 the reads go over
+ * NVLink-C2C).
+ *   host_block_map: int32 [layout.num_blocks] device array; -1 = the block's
+ *     records are in `pool`, h >= 0 = they are host block h of host_records
+ *   host_records: host-tier records, [n_host_blocks][n_layers][block_size]
+ *     records of layout.rec_stride bytes, 16-byte aligned, device-accessible
+ *     (e.g. cudaHostAlloc'd)
+ *   other arguments and results as smla_attend.  A map entry >= n_host_blocks
+ *   is latched as SMLA_ERR_BAD_INDEX and the record reads as zeros.
+ */
+smla_status_t smla_attend_hisparse(const smla_layout_t* layout, const smla_params_t* params, const void* pool,
+                                   int layer, const void* host_records, const int32_t* host_block_map,
+                                   int64_t n_host_blocks, const void* q, const void* q_pe, const int32_t* topk_idx,
+                                   const int32_t* block_table, int bt_stride, const int32_t* query_start_loc,
+                                   int batch, int n_tokens, void* out, float* lse, void* stream);
+
+/*
  * smla_decode -- one step of the whole path for one layer:
  * kvpack_store(new tokens) -> smla_index_scores -> smla_topk -> smla_attend.
  * Serves decode steps with MTP drafts ([GLM-5.3 "Config and numbers"]: MTP3)

@@ -18,13 +18,13 @@ __all__ = [
     "SmlaError", "Layout", "Params", "lib", "layout_init", "workspace_size", "kvpack_store",
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
     "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static", "smla_prefill_chunk",
-    "smla_dcp_topk_merge", "smla_lse_merge",
+    "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
-    "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge",
+    "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
@@ -87,6 +87,7 @@ def lib() -> ctypes.CDLL:
             "smla_prefill_chunk": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
                                         _I, _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "smla_dcp_topk_merge": (_I, [_P, _I64, _I64, _P, _I, _I, _I, _P, _P, _P]),
+            "smla_attend_hisparse": (_I, [LP, PP, _P, _I, _P, _P, _I64, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P]),
             "smla_lse_merge": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
             "smla_get_last_error": (_I, [_P]),
             "smla_status_string": (ctypes.c_char_p, [_I]),
@@ -192,6 +193,25 @@ def smla_attend(layout, params, pool, layer, q, q_pe, topk_idx, block_table, que
                              _ptr(topk_idx), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
                              query_start_loc.numel() - 1, q.shape[0], _ptr(out), _ptr(lse), _stream(stream)),
            "smla_attend")
+
+
+def smla_attend_hisparse(layout, params, pool, layer, host_records, host_block_map, q, q_pe, topk_idx, block_table,
+                         query_start_loc, out, lse, stream=None):
+    """smla_attend with the records of mapped blocks read from a pinned host buffer (host_records, uint8)."""
+    _expect(q, torch.bfloat16, "q")
+    _expect(host_block_map, torch.int32, "host_block_map")
+    _expect(host_records, torch.uint8, "host_records")
+    if host_records.is_cuda or not host_records.is_pinned():
+        raise ValueError("host_records must be pinned host memory")
+    if not host_block_map.is_cuda:
+        raise ValueError("host_block_map must be a CUDA tensor")
+    rec_bytes = layout.n_layers * layout.block_size * layout.rec_stride
+    n_host = host_records.numel() // rec_bytes
+    _check(lib().smla_attend_hisparse(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer,
+                                      ctypes.c_void_p(host_records.data_ptr()), _ptr(host_block_map), n_host, _ptr(q),
+                                      _ptr(q_pe), _ptr(topk_idx), _ptr(block_table), block_table.shape[1],
+                                      _ptr(query_start_loc), query_start_loc.numel() - 1, q.shape[0], _ptr(out),
+                                      _ptr(lse), _stream(stream)), "smla_attend_hisparse")
 
 
 def smla_decode(layout, params, pool, layer, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping, q, q_pe,

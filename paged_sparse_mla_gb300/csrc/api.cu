@@ -196,6 +196,27 @@ smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* para
                        static_cast<cudaStream_t>(stream), d->err);
 }
 
+smla_status_t smla_attend_hisparse(const smla_layout_t* layout, const smla_params_t* params, const void* pool,
+                                   int layer, const void* host_records, const int32_t* host_block_map,
+                                   int64_t n_host_blocks, const void* q, const void* q_pe, const int32_t* topk_idx,
+                                   const int32_t* block_table, int bt_stride, const int32_t* query_start_loc,
+                                   int batch, int n_tokens, void* out, float* lse, void* stream) {
+  if (!layout_ok(layout) || !params || layer < 0 || layer >= layout->n_layers || batch <= 0 || n_tokens < 0 ||
+      params->top_k <= 0 || params->n_heads <= 0 || n_host_blocks < 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (n_tokens == 0) return SMLA_OK;
+  if (!pool || !q || (layout->d_rope > 0 && !q_pe) || !topk_idx || !block_table || !query_start_loc || !out || !lse ||
+      bt_stride <= 0 || !host_block_map || (n_host_blocks > 0 && !host_records) ||
+      (reinterpret_cast<uintptr_t>(host_records) & 15) != 0)
+    return SMLA_ERR_INVALID_ARG;
+  DeviceInfo* d;
+  smla_status_t st = check_device(&d);
+  if (st != SMLA_OK) return st;
+  return launch_attend(kernel_layout(*layout), params->n_heads, params->top_k, params->softmax_scale, pool, layer, q,
+                       q_pe, topk_idx, block_table, bt_stride, query_start_loc, batch, 0, n_tokens, out, lse,
+                       static_cast<cudaStream_t>(stream), d->err, host_records, host_block_map, n_host_blocks);
+}
+
 smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* params, void* pool, int layer,
                           const void* new_latent, const void* new_rope, const uint8_t* new_idx_k,
                           const float* new_idx_scale, const int64_t* slot_mapping, const void* q, const void* q_pe,

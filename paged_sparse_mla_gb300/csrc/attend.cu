@@ -89,6 +89,11 @@ struct AttnArgs {
   __nv_bfloat16* out;
   float* lse;
   unsigned* err;
+  // host tier: records of block b live at host_records + (host_block_map[b] * n_layers + layer) *
+  // block_size * rec_stride when host_block_map[b] >= 0 (nullptr map = every record in the pool)
+  const uint8_t* host_records;
+  const int32_t* host_block_map;
+  int64_t n_host_blocks;
 };
 
 // Transpose-reduce 32 per-lane values across the 32 lanes of a warp: afterwards
@@ -346,6 +351,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         if (blk < 0 || blk >= L.num_blocks) {
           latch_error(A.err, SMLA_ERR_BAD_INDEX);
           return nullptr;
+        }
+        if (A.host_block_map != nullptr) {
+          const int hb = __ldg(A.host_block_map + blk);
+          if (hb >= 0) {  // the record lives in the host tier (read over the CPU-GPU link)
+            if (hb >= A.n_host_blocks) {
+              latch_error(A.err, SMLA_ERR_BAD_INDEX);
+              return nullptr;
+            }
+            return A.host_records +
+                   ((static_cast<int64_t>(hb) * L.n_layers + A.layer) * L.block_size + j % L.block_size) * L.rec_stride;
+          }
         }
         return A.pool + static_cast<int64_t>(blk) * L.block_stride + static_cast<int64_t>(A.layer) * L.layer_stride +
                L.rec_off + static_cast<int64_t>(j % L.block_size) * L.rec_stride;
@@ -759,7 +775,8 @@ smla_status_t launch_nch(const AttnArgs& A, cudaStream_t stream) {
 smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float softmax_scale, const void* pool,
                             int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
                             const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
-                            int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err) {
+                            int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err,
+                            const void* host_records, const int32_t* host_block_map, int64_t n_host_blocks) {
   if (tok_end <= tok_begin) return SMLA_OK;
   if (n_heads > kHeads || L.d_rope > 64 || L.d_latent % 64 != 0) return SMLA_ERR_UNSUPPORTED;
   AttnArgs A;
@@ -781,6 +798,9 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
   A.out = static_cast<__nv_bfloat16*>(out);
   A.lse = lse;
   A.err = err;
+  A.host_records = static_cast<const uint8_t*>(host_records);
+  A.host_block_map = host_block_map;
+  A.n_host_blocks = n_host_blocks;
   switch (L.d_latent / 64) {
     case 1: return launch_nch<2, false>(A, stream);
     case 8: {

@@ -55,6 +55,8 @@ smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride,
 smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float softmax_scale, const void* pool,
                             int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
                             const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
-                            int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err);
+                            int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err,
+                            const void* host_records = nullptr, const int32_t* host_block_map = nullptr,
+                            int64_t n_host_blocks = 0);
 
 }  // namespace smla

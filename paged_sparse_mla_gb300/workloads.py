@@ -306,3 +306,30 @@ def shard_pools(wl: Workload, layout, pool: torch.Tensor, n_shards: int, *, seed
                            seq_lens=torch.as_tensor(np.asarray(lr, dtype=np.int32), device=dev),
                            max_ctx=max(1, max(lr))))
     return shards
+
+
+# ----------------------------------------------------------------------------- host tier
+def evict_records(layout, pool: torch.Tensor, blocks, *, chunk: int = 256):
+    """Move the latent records of `blocks` (every layer) to pinned host memory.
+
+    Returns (host_records uint8 pinned [n * n_layers * block_size * rec_stride],
+    host_block_map int32 [num_blocks] on the pool's device: -1 = in the pool,
+    h = host block h).  The moved regions are zeroed in the pool; indexer keys
+    and scales stay.
+    """
+    dev = pool.device
+    blocks = torch.as_tensor(np.asarray(blocks, dtype=np.int64), device=dev)
+    per = layout.block_size * layout.rec_stride
+    n = blocks.numel()
+    host = torch.empty(n * layout.n_layers * per, dtype=torch.uint8).pin_memory()
+    hmap = torch.full((layout.num_blocks,), -1, dtype=torch.int32, device=dev)
+    hmap[blocks] = torch.arange(n, dtype=torch.int32, device=dev)
+    ar = torch.arange(per, device=dev, dtype=torch.int64)
+    view = host.view(n, layout.n_layers, per)  # host layout [block][layer][records]
+    for c0 in range(0, n, chunk):
+        b = blocks[c0:c0 + chunk]
+        for layer in range(layout.n_layers):
+            idx = ((b * layout.block_stride + layer * layout.layer_stride + layout.rec_off)[:, None] + ar).reshape(-1)
+            view[c0:c0 + b.numel(), layer].copy_(pool[idx].reshape(b.numel(), per).cpu())
+            pool[idx] = 0
+    return host, hmap
