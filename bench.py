@@ -305,31 +305,55 @@ def run_gpu(args):
     host_in = {n: getattr(wl, n).cpu().pin_memory() for n in
                ("new_latent", "new_rope", "new_idx_k", "new_idx_s", "slot_mapping", "q", "q_pe", "q_idx", "w",
                 "block_table", "seq_lens", "query_start_loc")}
-    dev_in = {n: torch.empty_like(v, device="cuda") for n, v in host_in.items()}
-    host_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    host_lse = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    # Two sets of device inputs/outputs: the copies of one step (inputs on `copy`, results on
+    # `back`) overlap the neighbouring steps' kernels (on `stream`); every step still moves its own
+    # inputs in and its own out/lse back inside the timed region.
+    dev_in = [{n: torch.empty_like(v, device="cuda") for n, v in host_in.items()} for _ in range(2)]
+    dev_out = [out, torch.empty_like(out)]
+    dev_lse = [lse, torch.empty_like(lse)]
+    host_out = [torch.empty(out.shape, dtype=out.dtype).pin_memory() for _ in range(2)]
+    host_lse = [torch.empty(lse.shape, dtype=lse.dtype).pin_memory() for _ in range(2)]
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = host_out.numel() * host_out.element_size() + host_lse.numel() * host_lse.element_size()
+    d2h = host_out[0].numel() * host_out[0].element_size() + host_lse[0].numel() * host_lse[0].element_size()
+    copy = torch.cuda.Stream()      # host -> device
+    back = torch.cuda.Stream()      # device -> host (separate, so the next inputs need not wait for it)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_read = [torch.cuda.Event() for _ in range(2)]
+    for b in range(2):  # nothing to wait for before the first use of each buffer
+        ev_done[b].record(stream)
+        ev_read[b].record(back)
 
-    def e2e_step():
-        for n, v in host_in.items():
-            dev_in[n].copy_(v, non_blocking=True)
-        smla.smla_decode(lay, prm, pool, 0, dev_in["new_latent"], dev_in["new_rope"], dev_in["new_idx_k"],
-                         dev_in["new_idx_s"], dev_in["slot_mapping"], dev_in["q"], dev_in["q_pe"], dev_in["q_idx"],
-                         dev_in["w"], dev_in["block_table"], dev_in["seq_lens"], dev_in["query_start_loc"],
-                         wl.max_q, wl.max_ctx, out, lse, ws, topk_idx_out=topk, stream=stream)
-        host_out.copy_(out, non_blocking=True)
-        host_lse.copy_(lse, non_blocking=True)
+    def e2e_step(i):
+        b = i & 1
+        d = dev_in[b]
+        copy.wait_event(ev_done[b])              # step i-2's kernels are done with these inputs
+        with torch.cuda.stream(copy):
+            for n, v in host_in.items():
+                d[n].copy_(v, non_blocking=True)
+        ev_in[b].record(copy)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_read[b])            # step i-2's results were read back
+        smla.smla_decode(lay, prm, pool, 0, d["new_latent"], d["new_rope"], d["new_idx_k"], d["new_idx_s"],
+                         d["slot_mapping"], d["q"], d["q_pe"], d["q_idx"], d["w"], d["block_table"],
+                         d["seq_lens"], d["query_start_loc"], wl.max_q, wl.max_ctx, dev_out[b], dev_lse[b], ws,
+                         topk_idx_out=topk, stream=stream)
+        ev_done[b].record(stream)
+        back.wait_event(ev_done[b])
+        with torch.cuda.stream(back):
+            host_out[b].copy_(dev_out[b], non_blocking=True)
+            host_lse[b].copy_(dev_lse[b], non_blocking=True)
+        ev_read[b].record(back)
 
-    for _ in range(args.warmup):
-        e2e_step()
+    for i in range(args.warmup):
+        e2e_step(i)
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
-    e0.record(stream)
-    for _ in range(args.steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(copy)
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record(back)                              # after the last step's results are read back
     torch.cuda.synchronize()
     ms_e2e = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = whole_job_rate(T, world, args.steps, ms_e2e)
