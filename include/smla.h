@@ -317,6 +317,16 @@ smla_status_t smla_dcp_topk_merge(const float* shard_scores, int64_t shard_strid
 smla_status_t smla_lse_merge(const void* parts_out, const float* parts_lse, int n_shards, int n_tokens,
                              int n_heads, int d, void* out, float* lse, void* stream);
 
+/* Self-check of the on-device wait bound and of the pipelined kernels' exit
+ * protocol.  One CTA of four warps: warp 0 waits on an mbarrier that no thread
+ * ever arrives at, warps 1-3 on one that completes; the failed wait gives up
+ * after `limit_ns` nanoseconds (1 ms .. 10 s of %globaltimer), latches
+ * SMLA_ERR_TIMEOUT in the device error word and is ORed into the group barrier,
+ * so that all four warps leave together and the kernel returns.  The caller reads
+ * the status with smla_get_last_error(); the context stays usable.  Returns
+ * SMLA_ERR_INVALID_ARG for a limit outside the range, else the launch status. */
+smla_status_t smla_selftest_wait(int64_t limit_ns, void* stream);
+
 /* Synchronise `stream`, return the latched device error (and clear it). */
 smla_status_t smla_get_last_error(void* stream);
 

@@ -18,13 +18,14 @@ __all__ = [
     "SmlaError", "Layout", "Params", "lib", "layout_init", "workspace_size", "kvpack_store",
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
     "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static", "smla_prefill_chunk",
-    "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
+    "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse", "smla_selftest_wait",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
     "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
+    "smla_selftest_wait",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
@@ -89,6 +90,7 @@ def lib() -> ctypes.CDLL:
             "smla_dcp_topk_merge": (_I, [_P, _I64, _I64, _P, _I, _I, _I, _P, _P, _P]),
             "smla_attend_hisparse": (_I, [LP, PP, _P, _I, _P, _P, _I64, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P]),
             "smla_lse_merge": (_I, [_P, _P, _I, _I, _I, _I, _P, _P, _P]),
+            "smla_selftest_wait": (_I, [_I64, _P]),
             "smla_get_last_error": (_I, [_P]),
             "smla_status_string": (ctypes.c_char_p, [_I]),
             "smla_version": (_I, []),
@@ -279,6 +281,11 @@ def smla_lse_merge(parts_out, parts_lse, out, lse, stream=None):
     n, t, h, d = parts_out.shape
     _check(lib().smla_lse_merge(_ptr(parts_out), _ptr(parts_lse), n, t, h, d, _ptr(out), _ptr(lse), _stream(stream)),
            "smla_lse_merge")
+
+
+def smla_selftest_wait(limit_ns, stream=None):
+    """Launch the bounded-wait self-check (one wait never completes; it gives up after limit_ns)."""
+    _check(lib().smla_selftest_wait(int(limit_ns), _stream(stream)), "smla_selftest_wait")
 
 
 def smla_get_last_error(stream=None) -> int:

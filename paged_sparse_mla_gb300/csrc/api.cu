@@ -14,6 +14,28 @@ constexpr size_t kScoreBudget = size_t(512) << 20;  // bytes of fp32 scores per 
 
 inline int64_t round_up(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
+// The exit protocol of the warp-specialised kernels on a barrier that never
+// completes: warp 0 waits on bar[0], which no thread arrives at; warps 1-3 wait
+// on bar[1], whose first phase thread 32 completes.  The failed wait is made
+// warp-uniform and ORed into the group barrier, so that the four warps leave
+// together.
+__global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
+  __shared__ uint64_t bar[2];
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar[0], 1);
+    mbar_init(&bar[1], 1);
+    abort_flag = 0;
+    mbar_fence_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 32) mbar_arrive(&bar[1]);
+  const int warp = threadIdx.x >> 5;
+  volatile int* abort = &abort_flag;
+  const bool ok = __all_sync(0xffffffffu, mbar_wait(&bar[warp == 0 ? 0 : 1], 0, err, abort, limit_ns));
+  bar_red_or(1, 128, !ok);
+}
+
 struct DeviceInfo {
   bool init = false;
   int sms = 0;
@@ -278,6 +300,14 @@ smla_status_t smla_prefill_chunk(const smla_layout_t* layout, const smla_params_
   return smla_decode(layout, params, pool, layer, chunk_latent, chunk_rope, chunk_idx_k, chunk_idx_scale, slot_mapping,
                      q, q_pe, q_idx, w, block_table, bt_stride, seq_lens, query_start_loc, batch, n_tokens, chunk_len,
                      max_ctx, out, lse, topk_idx_out, workspace, workspace_bytes, stream);
+}
+
+smla_status_t smla_selftest_wait(int64_t limit_ns, void* stream) {
+  if (limit_ns < 1000000 || limit_ns > 10000000000ll) return SMLA_ERR_INVALID_ARG;
+  DeviceInfo* d = nullptr;
+  if (smla_status_t st = check_device(&d); st != SMLA_OK) return st;
+  wait_selftest_kernel<<<1, 128, 0, static_cast<cudaStream_t>(stream)>>>(d->err, static_cast<uint64_t>(limit_ns));
+  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
 smla_status_t smla_get_last_error(void* stream) {

@@ -141,18 +141,6 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return y;
 }
 
-// Barrier over `n` threads (named barrier `id`) that returns the OR of `pred`.
-__device__ __forceinline__ int bar_red_or(int id, int n, int pred) {
-  int r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
-      "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(pred), "r"(id), "r"(n)
-      : "memory");
-  return r;
-}
-
 // Eight bf16 values from 2-byte aligned memory; entries at or beyond `avail` read as zero.
 __device__ __forceinline__ uint4 load_bf16x8_padded(const uint16_t* src, int avail) {
   uint32_t w[4];
@@ -306,20 +294,29 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
     const bool rope16 = ((DL + 4 * L.n_scales) % 16) == 0;
     // WR: 512 latent codes, four per-128 scales and 64 rope values = 41 aligned 16-byte pieces
     constexpr bool whole_records = WR;
-    for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
+    // A failed wait never makes one warp leave alone: the thread carries on to the next
+    // group barrier (what it writes meanwhile is discarded), where the failure is ORed in
+    // (bar.red), so that every producer warp leaves the loop together and none is left
+    // waiting at a named barrier.
+    for (int tr = blockIdx.x; tr < A.n_rows; tr += gridDim.x, ++n) {
       const int t = A.tok_begin + tr;
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
       const int ntiles = row_tiles(idx, A.top_k, lane);
-      if (warp == kFirstProducerWarp && lane == 0) {
-        if (!mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) break;
-        sm.ntiles[n & 1] = ntiles;
-        mbar_arrive(&sm.tok_full[n & 1]);
+      bool fail = *abort != 0;
+      if (warp == kFirstProducerWarp && lane == 0 && !fail) {
+        if (mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) {
+          sm.ntiles[n & 1] = ntiles;
+          mbar_arrive(&sm.tok_full[n & 1]);
+        } else {
+          fail = true;
+        }
       }
+      if (bar_red_or(2, kProducerThreads, fail)) break;
       if (ntiles == 0) continue;
       const int b = seq_of_token(A.qsl, A.batch, t);
       const int32_t* bt = A.block_table + static_cast<int64_t>(b) * A.bt_stride;
       // ---- query -> swizzled bf16 chunks (heads and rope dims zero padded) ----
-      if (!mbar_wait(&sm.q_empty, (nw & 1) ^ 1, A.err, abort)) break;
+      const bool q_ok = mbar_wait(&sm.q_empty, (nw & 1) ^ 1, A.err, abort);
 #pragma unroll 4
       for (int u = ptid; u < kHeads * NCH * 8; u += kProducerThreads) {
         const int h = u / (NCH * 8), rem = u % (NCH * 8), c = rem / 8, v = rem % 8;
@@ -377,13 +374,14 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         sm.rec[0][ptid] = rec_of(j0, b0);
         sm.rec[1][ptid] = rec_of(j1, b1);
       }
-      named_bar_sync(2, kProducerThreads);
-      bool ok = true;
+      if (bar_red_or(2, kProducerThreads, !q_ok)) break;
+      bool failed = false;
       for (int tile = 0; tile < ntiles; ++tile, ++kk) {
         const int kb = kk & 1;
         const uint8_t* const* rec = sm.rec[tile % 3];
         const int j_ahead = entry(tile + 2);
         int blk_ahead = -1;
+        bool ok;
         if constexpr (whole_records) {
           // Whole-record gather: producer warp pw takes keys pw, pw + 11, ...; for each key,
           // lane l loads latent piece l (16 codes) and, for l < 9, the piece after the latent
@@ -430,10 +428,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           };
           constexpr int kNB = ((kTile + kPW - 1) / kPW + kR - 1) / kR;  // batches per tile
           load_batch(0, lat[0], ext[0]);
-          if (!mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort)) {
-            ok = false;
-            break;
-          }
+          ok = mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort);
 #pragma unroll
           for (int bi = 0; bi < kNB; ++bi) {
             if (bi + 1 < kNB) load_batch((bi + 1) * kR, lat[(bi + 1) & 1], ext[(bi + 1) & 1]);
@@ -445,10 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         uint4 cur[kBatch];
         float csc[kBatch];
         load_units(rec, ptid, n_lat, n_units, parts, DL, DR, L.quant_tile, L.n_scales, rope16, cur, csc);
-        if (!mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort)) {
-          ok = false;
-          break;
-        }
+        ok = mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort);
         for (int base = 0; base < n_units; base += kBatch * kProducerThreads) {
           uint4 nxt[kBatch];
           float nsc[kBatch];
@@ -487,9 +479,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         if (lane == 0) mbar_arrive(&sm.kv_full[kb]);
         // tile t+2's addresses after the hand-off: the block-table load must not delay the MMA
         if (ptid < kTile) sm.rec[(tile + 2) % 3][ptid] = rec_of(j_ahead, blk_ahead);
-        named_bar_sync(2, kProducerThreads);  // tile t+2's addresses complete; this tile's reads done
+        // tile t+2's addresses complete; this tile's reads done; any failed wait ends the row
+        if (bar_red_or(2, kProducerThreads, !ok)) {
+          failed = true;
+          break;
+        }
       }
-      if (!ok) break;
+      if (failed) break;
       ++nw;
     }
   } else if (warp == kMmaWarp) {
@@ -590,9 +586,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
     const int key = 16 * sp + lane;         // key of the tile (lanes < 16)
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
     uint32_t n = 0, nw = 0, kk = 0;
-    for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
+    // As in the producers, a failed wait skips nothing: the thread finishes the tile (what it
+    // computes is discarded) and the failure is ORed into the next group barrier, so that the
+    // eight warps leave together.
+    for (int tr = blockIdx.x; tr < A.n_rows; tr += gridDim.x, ++n) {
       const int t = A.tok_begin + tr;
-      if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
+      const bool go = *abort == 0 && mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort);
+      if (bar_red_or(1, kSoftmaxThreads, !go)) break;
       const int ntiles = sm.ntiles[n & 1];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tok_empty[n & 1]);
@@ -606,15 +606,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       float l_part[32];
 #pragma unroll
       for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
-      bool ok = true;
+      bool ok = true, failed = false;
       for (int tile = 0; tile < ntiles; ++tile, ++kk) {
         const int kb = kk & 1;
         const int e = tile * kTile + key;
         const bool valid = lane < 16 && e < A.top_k && __ldg(idx + e) >= 0;
-        if (!mbar_wait(&sm.s_full[kb], (kk >> 1) & 1, A.err, abort)) {
-          ok = false;
-          break;
-        }
+        ok = ok && mbar_wait(&sm.s_full[kb], (kk >> 1) & 1, A.err, abort);
         tc_fence_after();
         float sc[32];
         {
@@ -637,7 +634,12 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           }
           sm.red[sp][32 * hh + lane] = mine;
         }
-        named_bar_sync(1, kSoftmaxThreads);
+        // this tile's maxima are complete; a failed wait in any warp (here or in the
+        // previous tile's rescale) ends the token for all of them
+        if (bar_red_or(1, kSoftmaxThreads, !ok)) {
+          failed = true;
+          break;
+        }
         int need_h = 0;
         if (tid < kHeads) {
           const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
@@ -686,10 +688,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         // tile's buffer was released, and MMA2 of this tile waits for p_full below
         if (moved && tile > 0) {
           const uint32_t kp = kk - 1;
-          if (!mbar_wait(&sm.kv_empty[kp & 1], (kp >> 1) & 1, A.err, abort)) {
-            ok = false;
-            break;
-          }
+          ok = mbar_wait(&sm.kv_empty[kp & 1], (kp >> 1) & 1, A.err, abort) && ok;
           tc_fence_after();
 #pragma unroll 1
           for (int d2 = 0; d2 < kDTiles; ++d2) {
@@ -707,13 +706,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.p_full[kb]);
       }
-      if (!ok) break;
+      if (failed) break;
       // ---- end of token: row sums, normalisation, lse ----
-      if (!mbar_wait(&sm.o_done, nw & 1, A.err, abort)) break;
+      ok = ok && mbar_wait(&sm.o_done, nw & 1, A.err, abort);
       tc_fence_after();
       warp_transpose_reduce32<false>(l_part, lane);
       sm.red[sp][32 * hh + lane] = l_part[0];
-      named_bar_sync(1, kSoftmaxThreads);
+      if (bar_red_or(1, kSoftmaxThreads, !ok)) break;
       if (tid < kHeads) {
         const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
         sm.l_fin[tid] = 1.f / l;  // normalisation as one reciprocal per head

@@ -72,19 +72,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 
 // Wait for the phase of `bar` with the given parity to complete.  Returns
 // false (after latching SMLA_ERR_TIMEOUT and raising *abort) if it did not
-// complete within kWaitLimitNs, or if another role already aborted.
+// complete within limit_ns, or if another role already aborted.  The abort
+// flag and the clock are read every 16th poll only: a poll that fails is then
+// just the try_wait and a branch, which leaves the issue slots to the warps that
+// are working.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, unsigned* err,
-                                          volatile int* abort) {
+                                          volatile int* abort, uint64_t limit_ns = kWaitLimitNs) {
   const uint32_t addr = smem_u32(bar);
-  if (mbar_try_wait(addr, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
     if (mbar_try_wait(addr, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-      latch_error(err, SMLA_ERR_TIMEOUT);
-      *abort = 1;
-      return false;
+    if ((i & 15u) == 15u) {
+      if (*abort) return false;
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > limit_ns) {
+        latch_error(err, SMLA_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
     }
   }
 }
@@ -120,6 +127,18 @@ __device__ __forceinline__ void fence_proxy_async() {
 
 __device__ __forceinline__ void named_bar_sync(int id, int n) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(n) : "memory");
+}
+
+// Barrier over `n` threads (named barrier `id`) that returns the OR of `pred`.
+__device__ __forceinline__ int bar_red_or(int id, int n, int pred) {
+  int r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.s32 p, %1, 0;\n\t"
+      "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.s32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(pred), "r"(id), "r"(n)
+      : "memory");
+  return r;
 }
 
 __device__ __forceinline__ void prefetch_l2_bulk(const void* p, uint32_t bytes) {

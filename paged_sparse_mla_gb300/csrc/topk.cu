@@ -12,7 +12,9 @@
 //   2. warp w scans its own contiguous segment of the row and appends every
 //      element with key >= T, as a 64-bit (key, ~position) pair, to its own list
 //      in shared memory, in position order (16 keys per lane per iteration, the
-//      next 16 in flight; one warp scan per iteration places the hits).
+//      next 16 in flight; one warp scan per iteration places the hits).  Bulk
+//      L2 prefetches run 16 KB ahead of each warp; the first are issued before
+//      the sample, so the segment starts arriving while T is chosen.
 // If at least k were collected and no list overflowed, a radix select over the
 // lists gives the exact k-th largest key; keys above it are kept and ties keep
 // their lowest positions.  Because the lists are position-ordered and the
@@ -34,6 +36,7 @@ constexpr int kSample = 8192;  // sample size for the threshold (runs of 4)
 constexpr int kMaxK = 4096;    // largest k of the fast path (power of two)
 constexpr int kWarpCap = kCap / kWarps;  // candidates per warp list (512)
 constexpr int kSpan = 32 * 16;           // positions a warp scans per iteration (16 per lane)
+constexpr int kPrefetchAhead = 4096;     // positions each warp keeps requested into L2 ahead of its scan
 
 struct TopkSmem {
   int hist[kBins];
@@ -276,6 +279,17 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     topk_slow(sm, s, n, k, o);
     return;
   }
+  // Segment of warp w in the collection pass below; its first kPrefetchAhead positions are
+  // requested into L2 now, so that they arrive while the threshold is being chosen.
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int seg = (n + kWarps * kSpan - 1) / (kWarps * kSpan) * kSpan;
+  const int p_lo = min(n, warp * seg), p_hi = min(n, p_lo + seg);
+  const bool aligned = (reinterpret_cast<uintptr_t>(s) & 15) == 0;
+  const auto prefetch = [&](int from, int to) {  // whole 16-byte granules of positions [from, to)
+    const int bytes = ((to - from) * 4) & ~15;
+    if (bytes > 0) prefetch_l2_bulk(s + from, static_cast<uint32_t>(bytes));
+  };
+  if (aligned && n > kCap && lane == 0) prefetch(p_lo, min(p_hi, p_lo + kPrefetchAhead));
   // ---- threshold from a sample (skipped when every position fits) ----
   uint32_t thr = 0;  // keep keys >= thr
   if (n > kCap) {
@@ -295,15 +309,13 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     int rem;
     thr = radix_select(sm, samp, kSample, want, rem, 2);  // 24 bits: the threshold's bin is kept whole
   }
-  if ((reinterpret_cast<uintptr_t>(s) & 15) != 0) {  // rows that are not 16-byte aligned
+  if (!aligned) {  // rows that are not 16-byte aligned
     topk_slow(sm, s, n, k, o);
     return;
   }
   // ---- one pass: warp w scans its own contiguous segment and appends every key >= thr, in
-  // position order, to its own list (16 keys per lane per iteration, the next 16 in flight) ----
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int seg = (n + kWarps * kSpan - 1) / (kWarps * kSpan) * kSpan;
-  const int p_lo = min(n, warp * seg), p_hi = min(n, p_lo + seg);
+  // position order, to its own list (16 keys per lane per iteration, the next 16 in flight,
+  // and the L2 request kPrefetchAhead positions ahead) ----
   unsigned long long* list = sm.cand + warp * kWarpCap;
   const auto load = [&](int p0, float4 (&v)[4]) {
 #pragma unroll
@@ -325,6 +337,8 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
     if (p_lo < p_hi) load(p_lo + 16 * lane, cur);
     for (int base = p_lo; base < p_hi; base += kSpan) {
       const int p0 = base + 16 * lane;
+      if (lane == 0 && base + kPrefetchAhead < p_hi)
+        prefetch(base + kPrefetchAhead, min(p_hi, base + kPrefetchAhead + kSpan));
       if (base + kSpan < p_hi) load(p0 + kSpan, nxt);
       uint32_t keys[16];
       uint32_t hit = 0;

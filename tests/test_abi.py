@@ -71,5 +71,7 @@ def test_host_side_argument_checks(lib):
                                   None, 1, 0, 4, 100, None, None, None, None, 0, None) == 0  # an empty chunk
     assert lib.smla_workspace_size(L, P, 0, 100) == 0
     assert lib.smla_workspace_size(L, P, 4, 1000) >= 4 * 1000 * 4 + 4 * 2048 * 4
+    assert lib.smla_selftest_wait(0, None) == 1                  # wait limit below 1 ms
+    assert lib.smla_selftest_wait(20_000_000_000, None) == 1     # above 10 s
     assert lib.smla_status_string(4) == b"SMLA_ERR_BAD_INDEX"
     assert lib.smla_version() >= 100

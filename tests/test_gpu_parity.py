@@ -203,6 +203,26 @@ def test_bad_block_id_is_reported_not_faulted():
     assert G.smla.smla_get_last_error() == 0        # cleared by the read
 
 
+def test_wait_that_never_completes_times_out_and_context_survives():
+    """A bounded wait on an mbarrier nothing arrives at gives up, reports SMLA_ERR_TIMEOUT and returns."""
+    import time
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    G.smla.smla_selftest_wait(50_000_000)           # 50 ms
+    assert G.smla.smla_get_last_error() == 5        # SMLA_ERR_TIMEOUT, read and cleared
+    assert time.perf_counter() - t0 >= 0.05
+    assert G.smla.smla_get_last_error() == 0
+    # the context still runs the path, with the oracle's result
+    wl = make_config(1)
+    ref = oracle_step(wl, oracle_pool(wl))
+    g = G.cuda_wl(make_config(1))
+    lay, prm = G.gpu_layout(g), G.gpu_params(g)
+    res = G.run_decode(g, G.gpu_pool(g, lay), lay, prm)
+    assert res["err"] == 0
+    for t in range(g.n_tokens):
+        assert np.array_equal(res["topk"][t], ref[t]["topk"])
+
+
 def test_bad_slot_is_reported_and_skipped():
     g = G.cuda_wl(make_config(1))
     lay = G.gpu_layout(g)
