@@ -191,8 +191,12 @@ def traffic_table():
 
 
 def source_sha(kernel):
-    p = os.path.join(ROOT, "paged_sparse_mla_gb300", "csrc", KERNEL_SOURCES[kernel])
-    return hashlib.sha256(open(p, "rb").read()).hexdigest()[:16]
+    """Hash of the kernel's source file and the device headers every kernel includes."""
+    csrc = os.path.join(ROOT, "paged_sparse_mla_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in (KERNEL_SOURCES[kernel], "smla_device.cuh", "smla_internal.h"):
+        h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()[:16]
 
 
 # ----------------------------------------------------------------------------- GPU arm

@@ -267,7 +267,7 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
     if (st != SMLA_OK) return st;
   }
   const int64_t stride = round_up(max_ctx, 4);
-  const int g = query_group(n_tokens, stride);
+  const int g = static_cast<int>(wave_aligned_group(query_group(n_tokens, stride), n_tokens));
   float* scores = static_cast<float*>(workspace);
   int32_t* topk_ws =
       reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + round_up(static_cast<int64_t>(g) * stride * 4, 256));

@@ -617,7 +617,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         {
           uint32_t r[32];
           tmem_ld32(tmem_s + lane_base + kb * kHeads + 32 * hh, r);
-          tmem_ld_wait();
+          tmem_ld_wait(r);
 #pragma unroll
           for (int h = 0; h < 32; ++h) sc[h] = valid ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
         }
@@ -694,7 +694,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
           for (int d2 = 0; d2 < kDTiles; ++d2) {
             uint32_t o[32];
             tmem_ld32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
-            tmem_ld_wait();
+            tmem_ld_wait(o);
 #pragma unroll
             for (int x = 0; x < 32; ++x) o[x] = __float_as_uint(__uint_as_float(o[x]) * sm.alpha[32 * hh + x]);
             tmem_st32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
@@ -724,7 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
         const int d = d2 * 128 + sp * 32 + lane;
         uint32_t o[32];
         tmem_ld32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
-        tmem_ld_wait();
+        tmem_ld_wait(o);
         if (d < DL) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {

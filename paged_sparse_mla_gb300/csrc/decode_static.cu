@@ -73,7 +73,7 @@ extern "C" smla_status_t smla_decode_static(const smla_layout_t* layout, const s
   const int64_t per_token = stride * 4 + static_cast<int64_t>(params->top_k) * 4;
   int64_t g = static_cast<int64_t>(kStaticScratchBytes - 512) / per_token;
   if (g < 1) return SMLA_ERR_SCRATCH_LIMIT;  // one token's score row and indices exceed the scratch
-  if (g > n_tokens) g = n_tokens;
+  g = wave_aligned_group(g, n_tokens);
   uint8_t* scratch = nullptr;
   smla_status_t st = static_scratch(&scratch);
   if (st != SMLA_OK) return st;

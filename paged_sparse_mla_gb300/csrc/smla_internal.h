@@ -48,6 +48,18 @@ smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const 
                                   int tok_end, int max_q, int max_ctx, float* scores, int64_t scores_stride,
                                   cudaStream_t stream, unsigned* err);
 
+// CTAs of the top-k kernel resident at once on the current device (0 if unknown).
+int topk_wave();
+
+// Query tokens per group, rounded down to whole waves of the top-k kernel (which
+// also gives the persistent attention grid a whole number of rows per CTA) when
+// the group is smaller than the batch.  `g` is the largest group the scratch holds.
+inline int64_t wave_aligned_group(int64_t g, int n_tokens) {
+  if (g >= n_tokens) return n_tokens;
+  const int wave = topk_wave();
+  return (wave > 0 && g >= wave) ? g - g % wave : g;
+}
+
 smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
                           const int32_t* query_start_loc, int batch, int tok_begin, int tok_end, int32_t* topk_idx,
                           cudaStream_t stream, unsigned* err);

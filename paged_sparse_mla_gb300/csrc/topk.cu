@@ -257,13 +257,10 @@ __device__ void topk_slow(TopkSmem& sm, const float* s, int n, int k, int32_t* o
   }
 }
 
-__global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __restrict__ scores, int64_t stride,
-                                                        const int32_t* __restrict__ seq_lens,
-                                                        const int32_t* __restrict__ qsl, int batch, int tok_begin,
-                                                        int32_t* __restrict__ out) {
-  extern __shared__ uint8_t smem_raw[];
-  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
-  const int row = blockIdx.x;
+// The top-k of one row (every thread of the CTA; each branch below is CTA-uniform).
+__device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__ scores, int64_t stride,
+                         const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl, int batch,
+                         int tok_begin, int32_t* __restrict__ out) {
   const int t = tok_begin + row;
   const int b = seq_of_token(qsl, batch, t);
   const int q0 = __ldg(qsl + b), n_q = __ldg(qsl + b + 1) - q0;
@@ -438,7 +435,46 @@ __global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __re
   }
 }
 
+// One CTA per row while the rows fit one wave of resident CTAs.  Beyond that the grid is
+// one wave and CTA c takes the rows c, 2G-1-c, 2G+c, 4G-1-c, ... (G = gridDim.x): every
+// pass over G rows runs in the opposite direction to the one before, so a CTA pairs a
+// front row with a back row.  In causal prefill, where a row's length grows with its
+// position, this evens the CTAs' work in the manner of front/back context pairing.
+__global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __restrict__ scores, int64_t stride,
+                                                        const int32_t* __restrict__ seq_lens,
+                                                        const int32_t* __restrict__ qsl, int batch, int tok_begin,
+                                                        int n_rows, int32_t* __restrict__ out) {
+  extern __shared__ uint8_t smem_raw[];
+  TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
+  const int G = static_cast<int>(gridDim.x);
+  for (int base = 0, pass = 0; base < n_rows; base += G, ++pass) {
+    const int row = base + ((pass & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+    if (row < n_rows) topk_row(sm, row, k, scores, stride, seq_lens, qsl, batch, tok_begin, out);
+    __syncthreads();  // shared memory is reused by the next row
+  }
+}
+
+
 }  // namespace
+
+int topk_wave() {
+  constexpr int kMaxDev = 64;
+  static int wave[kMaxDev] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
+  if (wave[dev] == 0) {
+    const size_t smem = sizeof(TopkSmem);
+    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+        cudaSuccess)
+      return 0;
+    int per_sm = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel, kThreads, smem) != cudaSuccess ||
+        per_sm <= 0)
+      return 0;
+    wave[dev] = per_sm * device_sm_count();
+  }
+  return wave[dev];
+}
 
 smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
                           const int32_t* query_start_loc, int batch, int tok_begin, int tok_end, int32_t* topk_idx,
@@ -446,16 +482,11 @@ smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride,
   (void)err;
   const int rows = tok_end - tok_begin;
   if (rows <= 0) return SMLA_OK;
-  const size_t smem = sizeof(TopkSmem);
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
-      return SMLA_ERR_CUDA;
-    attr_set = true;
-  }
-  topk_kernel<<<rows, kThreads, smem, stream>>>(top_k, scores, scores_stride, seq_lens, query_start_loc, batch,
-                                                tok_begin, topk_idx);
+  const int wave = topk_wave();
+  if (wave <= 0) return SMLA_ERR_CUDA;
+  const int grid = rows < wave ? rows : wave;
+  topk_kernel<<<grid, kThreads, sizeof(TopkSmem), stream>>>(top_k, scores, scores_stride, seq_lens, query_start_loc,
+                                                             batch, tok_begin, rows, topk_idx);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 

@@ -223,6 +223,25 @@ def test_wait_that_never_completes_times_out_and_context_survives():
         assert np.array_equal(res["topk"][t], ref[t]["topk"])
 
 
+def test_topk_more_rows_than_one_wave():
+    """1,000 causal rows of one sequence: the top-k grid is one resident wave and each CTA takes
+    a front row and a back row in alternate passes; every row must still equal the oracle's."""
+    rng = np.random.default_rng(91)
+    R, L, k = 1000, 12000, 2048
+    stride = L
+    scores = (rng.integers(-40, 41, size=(R, stride)).astype(np.float32) * np.float32(0.5))
+    seq_lens = torch.tensor([L], dtype=torch.int32, device="cuda")
+    qsl = torch.tensor([0, R], dtype=torch.int32, device="cuda")
+    prm = smla.make_params(64, 64, k, 1.0)
+    out = torch.full((R, k), -7, dtype=torch.int32, device="cuda")
+    smla.smla_topk(prm, torch.as_tensor(scores, device="cuda"), seq_lens, qsl, out)
+    assert smla.smla_get_last_error() == 0
+    got = out.cpu().numpy()
+    for t in range(R):
+        n = L - R + t + 1
+        assert np.array_equal(got[t], oracle.topk_select(scores[t, :n], k)), f"row {t}"
+
+
 def test_bad_slot_is_reported_and_skipped():
     g = G.cuda_wl(make_config(1))
     lay = G.gpu_layout(g)
