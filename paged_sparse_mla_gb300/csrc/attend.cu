@@ -496,15 +496,27 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       bool issued = false;
       const uint32_t idesc1 = make_idesc(kTile, kHeads, 1, 1, 0, 0);  // bf16, both K-major, M = 64 keys
       const uint32_t idesc2 = make_idesc(128, kHeads, 1, 1, 1, 1);    // bf16, both MN-major, M = 128 dims
-      const uint32_t q0 = smem_u32(sm.q[0]);
+      // Shared-memory descriptors are built once: an operand address that moves by `off`
+      // bytes moves the descriptor's start-address field (bits 0-13, address / 16) by off / 16,
+      // which stays inside the field for every shared-memory address.
+      const uint64_t dq = sw128_desc(smem_u32(sm.q[0]), 16, 1024);
+      const uint64_t dk10 = sw128_desc(smem_u32(sm.kv[0][0]), 16, 1024);
+      const uint64_t dk11 = sw128_desc(smem_u32(sm.kv[1][0]), 16, 1024);
+      const uint64_t dv20 = sw128_desc(smem_u32(sm.kv[0][0]), kChunkBytes, 1024);
+      const uint64_t dv21 = sw128_desc(smem_u32(sm.kv[1][0]), kChunkBytes, 1024);
+      const uint64_t dp20 = sw128_desc(smem_u32(sm.kv[0][kLatChunks]), kChunkBytes, 1024);
+      const uint64_t dp21 = sw128_desc(smem_u32(sm.kv[1][kLatChunks]), kChunkBytes, 1024);
       // MMA1 of global tile k1: S^T = Khat . q^T over 576 dims into S buffer k1 % 2.
       const auto mma1 = [&](uint32_t k1) {
         const int b1 = k1 & 1;
-        const uint32_t kv0 = smem_u32(sm.kv[b1][0]);
+        const uint64_t ka = b1 ? dk11 : dk10;
+        const uint32_t ts = tmem_s + b1 * kHeads;
+#pragma unroll
         for (int c = 0; c < NCH; ++c) {
+#pragma unroll
           for (int k4 = 0; k4 < 4; ++k4) {
-            mma_f16(tmem_s + b1 * kHeads, sw128_desc(kv0 + c * kChunkBytes + k4 * 32, 16, 1024),
-                    sw128_desc(q0 + c * kHeads * 128 + k4 * 32, 16, 1024), idesc1, (c | k4) != 0);
+            mma_f16(ts, ka + ((c * kChunkBytes + k4 * 32) >> 4), dq + ((c * kHeads * 128 + k4 * 32) >> 4), idesc1,
+                    (c | k4) != 0);
           }
         }
         mma_commit(&sm.s_full[b1]);
@@ -512,12 +524,13 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       // MMA2 of global tile k2: O^T += V^T . P^T over the tile's 64 keys.
       const auto mma2 = [&](uint32_t k2, bool first) {
         const int b2 = k2 & 1;
-        const uint32_t kv0 = smem_u32(sm.kv[b2][0]);
-        const uint32_t pt = smem_u32(sm.kv[b2][kLatChunks]);
+        const uint64_t va = b2 ? dv21 : dv20, pb = b2 ? dp21 : dp20;
+#pragma unroll
         for (int d2 = 0; d2 < kDTiles; ++d2) {
+#pragma unroll
           for (int k16 = 0; k16 < kTile / 16; ++k16) {
-            mma_f16(tmem_o + d2 * kHeads, sw128_desc(kv0 + 2 * d2 * kChunkBytes + k16 * 2048, kChunkBytes, 1024),
-                    sw128_desc(pt + k16 * 2048, kChunkBytes, 1024), idesc2, !(first && k16 == 0));
+            mma_f16(tmem_o + d2 * kHeads, va + ((2 * d2 * kChunkBytes + k16 * 2048) >> 4), pb + ((k16 * 2048) >> 4),
+                    idesc2, !(first && k16 == 0));
           }
         }
         mma_commit(&sm.kv_empty[b2]);
