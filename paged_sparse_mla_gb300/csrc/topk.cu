@@ -13,8 +13,9 @@
 //      element with key >= T, as a 64-bit (key, ~position) pair, to its own list
 //      in shared memory, in position order (16 keys per lane per iteration, the
 //      next 16 in flight; one warp scan per iteration places the hits).  Bulk
-//      L2 prefetches run 16 KB ahead of each warp; the first are issued before
-//      the sample, so the segment starts arriving while T is chosen.
+//      L2 prefetches run 16 KB ahead of each warp.  (Prefetching the start of
+//      each segment before the sample was measured: those lines were evicted
+//      before use and read again, +64 MB per launch and slower.)
 // If at least k were collected and no list overflowed, a radix select over the
 // lists gives the exact k-th largest key; keys above it are kept and ties keep
 // their lowest positions.  Because the lists are position-ordered and the
@@ -276,8 +277,7 @@ __device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__
     topk_slow(sm, s, n, k, o);
     return;
   }
-  // Segment of warp w in the collection pass below; its first kPrefetchAhead positions are
-  // requested into L2 now, so that they arrive while the threshold is being chosen.
+  // Segment of warp w in the collection pass below.
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int seg = (n + kWarps * kSpan - 1) / (kWarps * kSpan) * kSpan;
   const int p_lo = min(n, warp * seg), p_hi = min(n, p_lo + seg);
@@ -286,7 +286,6 @@ __device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__
     const int bytes = ((to - from) * 4) & ~15;
     if (bytes > 0) prefetch_l2_bulk(s + from, static_cast<uint32_t>(bytes));
   };
-  if (aligned && n > kCap && lane == 0) prefetch(p_lo, min(p_hi, p_lo + kPrefetchAhead));
   // ---- threshold from a sample (skipped when every position fits) ----
   uint32_t thr = 0;  // keep keys >= thr
   if (n > kCap) {
