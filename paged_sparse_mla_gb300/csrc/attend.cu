@@ -32,6 +32,8 @@
 //     as it is gathered (the next scores are computed while the softmax works).
 //   * Epilogue: O^T / l -> bf16 out[t, h, d] (thread = dim, coalesced) and
 //     lse = ln(sum) from the running max and the reduced row sums.
+#include <cstring>
+
 #include "smla_internal.h"
 
 namespace smla {
@@ -94,6 +96,9 @@ struct AttnArgs {
   const uint8_t* host_records;
   const int32_t* host_block_map;
   int64_t n_host_blocks;
+  // 1: the query tile is loaded by the tensor-memory-access unit (nine 2-D tensor-map copies of
+  // 64 heads x 64 dims, 128-byte swizzled as the MMA reads them); 0: by the producer threads
+  int q_tma;
 };
 
 // Transpose-reduce 32 per-lane values across the 32 lanes of a warp: afterwards
@@ -246,7 +251,9 @@ __device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
 }
 
 template <int NCH, bool WR>
-__global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
+__global__ void __launch_bounds__(kThreads, 1)
+    attend_kernel(const AttnArgs A, const __grid_constant__ CUtensorMap q_map,
+                  const __grid_constant__ CUtensorMap qpe_map) {
   extern __shared__ uint8_t smem_raw[];
   AttnSmem<NCH>& sm =
       *reinterpret_cast<AttnSmem<NCH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -269,7 +276,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       mbar_init(&sm.s_empty[i], kSoftmaxThreads / 32);   // scores read by every softmax warp
       mbar_init(&sm.p_full[i], kSoftmaxThreads / 32);    // P^T written by every softmax warp
     }
-    mbar_init(&sm.q_full, kProducerThreads / 32);
+    mbar_init(&sm.q_full, A.q_tma ? 1 : kProducerThreads / 32);  // the copy's arrive, or one per warp
     mbar_init(&sm.q_empty, 1);
     mbar_init(&sm.o_done, 1);
     mbar_init(&sm.final_bar, 1);
@@ -290,6 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
     const int ptid = threadIdx.x - 32 * kFirstProducerWarp;  // 0..351
     uint32_t n = 0, nw = 0, kk = 0;
+    uint32_t q_issued = 0;  // query-tile copies issued by this thread (ptid 0 on the copy path)
     constexpr int parts = DL / 16;       // 16-code parts per record
     const bool rope16 = ((DL + 4 * L.n_scales) % 16) == 0;
     // WR: 512 latent codes, four per-128 scales and 64 rope values = 41 aligned 16-byte pieces
@@ -317,6 +325,17 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       const int32_t* bt = A.block_table + static_cast<int64_t>(b) * A.bt_stride;
       // ---- query -> swizzled bf16 chunks (heads and rope dims zero padded) ----
       const bool q_ok = mbar_wait(&sm.q_empty, (nw & 1) ^ 1, A.err, abort);
+      if (A.q_tma) {
+        // one thread issues the nine tile copies; their bytes complete q_full
+        if (ptid == 0 && q_ok) {
+          mbar_arrive_expect_tx(&sm.q_full, NCH * kChunkBytes);
+          const int y = t * A.n_heads;
+#pragma unroll
+          for (int c = 0; c < kLatChunks; ++c) tma_load_2d(smem_u32(sm.q[c]), &q_map, c * 64, y, &sm.q_full);
+          tma_load_2d(smem_u32(sm.q[kLatChunks]), &qpe_map, 0, y, &sm.q_full);
+          ++q_issued;
+        }
+      } else {
 #pragma unroll 4
       for (int u = ptid; u < kHeads * NCH * 8; u += kProducerThreads) {
         const int h = u / (NCH * 8), rem = u % (NCH * 8), c = rem / 8, v = rem % 8;
@@ -335,6 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       fence_proxy_async();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.q_full);
+      }
       // ---- key tiles ----
       // Unit stream of one tile: units [0, 64*parts) are 16-code latent pieces,
       // units [64*parts, 64*(parts+8)) are 16-byte rope pieces (see latent_unit).
@@ -488,6 +508,8 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
       if (failed) break;
       ++nw;
     }
+    // Leave only after the last query-tile copy has landed (it has, unless a wait gave up).
+    if (q_issued > 0) mbar_drain(&sm.q_full, (q_issued - 1) & 1);
   } else if (warp == kMmaWarp) {
     // ------------------------------ MMA issuer ------------------------------
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kOtherRegs));
@@ -763,7 +785,7 @@ __global__ void __launch_bounds__(kThreads, 1) attend_kernel(const AttnArgs A) {
 }
 
 template <int NCH, bool WR>
-smla_status_t launch_nch(const AttnArgs& A, cudaStream_t stream) {
+smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem<NCH>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
@@ -777,8 +799,34 @@ smla_status_t launch_nch(const AttnArgs& A, cudaStream_t stream) {
     if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set = true;
   }
+  // Query tiles by tensor-map copies when they match the shared-memory tile exactly: 64 heads,
+  // 64-dim chunks (the latent in NCH - 1 of them, the rope in one), 16-byte aligned rows.
+  CUtensorMap q_map, qpe_map;
+  std::memset(&q_map, 0, sizeof(q_map));
+  std::memset(&qpe_map, 0, sizeof(qpe_map));
+  A.q_tma = 0;
+  constexpr int DL = (NCH - 1) * 64;
+  if (A.n_heads == kHeads && A.L.d_rope == 64 && (reinterpret_cast<uintptr_t>(A.q) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(A.q_pe) & 15) == 0) {
+    EncodeTiledFn enc = encode_tiled();
+    const cuuint64_t rows = static_cast<cuuint64_t>(A.tok_begin + A.n_rows) * A.n_heads;
+    const cuuint64_t q_dims[2] = {static_cast<cuuint64_t>(DL), rows};
+    const cuuint64_t q_strides[1] = {static_cast<cuuint64_t>(DL) * 2};
+    const cuuint64_t pe_dims[2] = {64, rows};
+    const cuuint64_t pe_strides[1] = {128};
+    const cuuint32_t box[2] = {64, kHeads};
+    const cuuint32_t estr[2] = {1, 1};
+    if (enc != nullptr &&
+        enc(&q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(A.q), q_dims, q_strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS &&
+        enc(&qpe_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<__nv_bfloat16*>(A.q_pe), pe_dims, pe_strides,
+            box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
+      A.q_tma = 1;
+  }
   const int grid = min(A.n_rows, device_sm_count());
-  attend_kernel<NCH, WR><<<grid, kThreads, smem, stream>>>(A);
+  attend_kernel<NCH, WR><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 

@@ -2,6 +2,7 @@
 #pragma once
 
 #include <cstdint>
+#include <cuda.h>
 #include <cuda_runtime.h>
 
 #include "smla.h"
@@ -33,6 +34,12 @@ inline KernelLayout kernel_layout(const smla_layout_t& l) {
   k.block_stride = l.block_stride;
   return k;
 }
+
+// cuTensorMapEncodeTiled, looked up once through the runtime's driver entry point (nullptr if absent).
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+EncodeTiledFn encode_tiled();
 
 // Device error word (defined in api.cu); launchers receive its address.
 unsigned* device_error_word();
