@@ -281,6 +281,9 @@ def run_gpu(args):
     kern = {k: [] for k in ("kvpack_store", "smla_index_scores", "smla_topk", "smla_attend")}
     # one launch of each kernel over all query tokens (the fused call splits long prefill into groups)
     scores = torch.empty((T, stride), dtype=torch.float32, device="cuda")
+    # the attention's split scratch, as the fused step gives it (small batches split rows over CTAs)
+    att_ws_bytes = smla.attend_workspace_size(lay, prm, T)
+    att_ws = torch.empty(max(att_ws_bytes, 1), dtype=torch.uint8, device="cuda") if att_ws_bytes else None
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for it in range(args.warmup + args.steps):
         # keep the GPU busy while the host enqueues the four launches, so no host gap lands between events
@@ -295,7 +298,7 @@ def run_gpu(args):
         smla.smla_topk(prm, scores, wl.seq_lens, wl.query_start_loc, topk, stream=stream)
         ev[3].record(stream)
         smla.smla_attend(lay, prm, pool, 0, wl.q, wl.q_pe, topk, wl.block_table, wl.query_start_loc, out, lse,
-                         stream=stream)
+                         stream=stream, workspace=att_ws)
         ev[4].record(stream)
         torch.cuda.synchronize()
         if it >= args.warmup:

@@ -110,7 +110,8 @@ smla_status_t smla_layout_init(smla_layout_t* layout, int block_size, int n_laye
                                int d_rope, int quant_tile, int d_index, int64_t num_blocks);
 
 /* Bytes of `workspace` that smla_decode needs for these sizes (scores + top-k
- * scratch, 256-byte aligned pieces).  max_ctx = the largest seq_lens entry. */
+ * scratch, then the split-attention scratch of smla_attend_workspace_size,
+ * 256-byte aligned pieces).  max_ctx = the largest seq_lens entry. */
 size_t smla_workspace_size(const smla_layout_t* layout, const smla_params_t* params,
                            int n_tokens, int max_ctx);
 
@@ -174,11 +175,22 @@ smla_status_t smla_topk(const smla_params_t* params, const float* scores, int64_
  *   topk_idx int32 [n_tokens, top_k]; entries < 0 are ignored
  *   out      bf16 [n_tokens, n_heads, d_latent]
  *   lse      fp32 [n_tokens, n_heads]  (natural log; -inf and out = 0 when no entry is valid)
+ *   workspace, workspace_bytes: optional device scratch (NULL and 0 allowed).  With fewer
+ *     query tokens than SMs and at least smla_attend_workspace_size() bytes, each token's
+ *     selected positions are split into contiguous ranges over several CTAs (one wave in
+ *     all); every range yields a normalised fp32 partial output and its lse in the scratch,
+ *     and a merge kernel combines them as lse = ln sum_r exp(lse_r),
+ *     out = sum_r exp(lse_r - lse) out_r.  Without it, each token runs on one CTA.
  */
 smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* params, const void* pool,
                           int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
                           const int32_t* block_table, int bt_stride, const int32_t* query_start_loc,
-                          int batch, int n_tokens, void* out, float* lse, void* stream);
+                          int batch, int n_tokens, void* out, float* lse, void* workspace,
+                          size_t workspace_bytes, void* stream);
+
+/* Scratch bytes with which smla_attend splits the tokens' ranges over CTAs (0 when
+ * n_tokens is too large to need it). */
+size_t smla_attend_workspace_size(const smla_layout_t* layout, const smla_params_t* params, int n_tokens);
 
 /*
  * smla_attend_hisparse -- smla_attend with a host tier for the selected

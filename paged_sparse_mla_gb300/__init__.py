@@ -19,13 +19,14 @@ __all__ = [
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
     "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static", "smla_prefill_chunk",
     "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse", "smla_selftest_wait",
+    "attend_workspace_size",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
     "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
-    "smla_selftest_wait",
+    "smla_selftest_wait", "smla_attend_workspace_size",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
@@ -80,7 +81,8 @@ def lib() -> ctypes.CDLL:
             "kvpack_store": (_I, [LP, _P, _I, _P, _P, _P, _P, _P, _I, _P]),
             "smla_index_scores": (_I, [LP, PP, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _I64, _P]),
             "smla_topk": (_I, [PP, _P, _I64, _P, _P, _I, _I, _P, _P]),
-            "smla_attend": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P]),
+            "smla_attend": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P, ctypes.c_size_t, _P]),
+            "smla_attend_workspace_size": (ctypes.c_size_t, [LP, PP, _I]),
             "smla_decode": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I,
                                  _I, _I, _P, _P, _P, _P, ctypes.c_size_t, _P]),
             "smla_decode_static": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I,
@@ -185,15 +187,23 @@ def smla_topk(params, scores, seq_lens, query_start_loc, topk_idx, stream=None):
                            _stream(stream)), "smla_topk")
 
 
+def attend_workspace_size(layout, params, n_tokens) -> int:
+    return int(lib().smla_attend_workspace_size(ctypes.byref(layout), ctypes.byref(params), n_tokens))
+
+
 def smla_attend(layout, params, pool, layer, q, q_pe, topk_idx, block_table, query_start_loc, out, lse,
-                stream=None):
+                stream=None, workspace=None):
+    """Latent attention over the selected positions.  `workspace` (uint8 device tensor of at least
+    attend_workspace_size(...) bytes, optional) lets a small batch split each token over CTAs."""
     _expect(q, torch.bfloat16, "q")
     _expect(q_pe, torch.bfloat16, "q_pe")
     _expect(out, torch.bfloat16, "out")
     _expect(lse, torch.float32, "lse")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().smla_attend(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(q), _ptr(q_pe),
                              _ptr(topk_idx), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
-                             query_start_loc.numel() - 1, q.shape[0], _ptr(out), _ptr(lse), _stream(stream)),
+                             query_start_loc.numel() - 1, q.shape[0], _ptr(out), _ptr(lse), _ptr(workspace),
+                             ws_bytes, _stream(stream)),
            "smla_attend")
 
 

@@ -150,7 +150,14 @@ size_t smla_workspace_size(const smla_layout_t* layout, const smla_params_t* par
   const int64_t stride = round_up(max_ctx, 4);
   const int g = query_group(n_tokens, stride);
   return static_cast<size_t>(round_up(static_cast<int64_t>(g) * stride * 4, 256) +
-                             round_up(static_cast<int64_t>(g) * params->top_k * 4, 256));
+                             round_up(static_cast<int64_t>(g) * params->top_k * 4, 256)) +
+         smla_attend_workspace_size(layout, params, g);
+}
+
+size_t smla_attend_workspace_size(const smla_layout_t* layout, const smla_params_t* params, int n_tokens) {
+  if (!layout_ok(layout) || params == nullptr || n_tokens <= 0 || params->n_heads <= 0) return 0;
+  // rows fewer than the SMs are split; rows x splits stay within kMaxSplitUnits (>= any SM count)
+  return n_tokens < kMaxSplitUnits ? attend_split_bytes(params->n_heads, layout->d_latent, kMaxSplitUnits) : 0;
 }
 
 smla_status_t kvpack_store(const smla_layout_t* layout, void* pool, int layer, const void* latent, const void* rope,
@@ -202,9 +209,9 @@ smla_status_t smla_topk(const smla_params_t* params, const float* scores, int64_
 smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* params, const void* pool, int layer,
                           const void* q, const void* q_pe, const int32_t* topk_idx, const int32_t* block_table,
                           int bt_stride, const int32_t* query_start_loc, int batch, int n_tokens, void* out,
-                          float* lse, void* stream) {
+                          float* lse, void* workspace, size_t workspace_bytes, void* stream) {
   if (!layout_ok(layout) || !params || layer < 0 || layer >= layout->n_layers || batch <= 0 || n_tokens < 0 ||
-      params->top_k <= 0 || params->n_heads <= 0)
+      params->top_k <= 0 || params->n_heads <= 0 || (workspace == nullptr && workspace_bytes != 0))
     return SMLA_ERR_INVALID_ARG;
   if (n_tokens == 0) return SMLA_OK;
   if (!pool || !q || (layout->d_rope > 0 && !q_pe) || !topk_idx || !block_table || !query_start_loc || !out || !lse ||
@@ -215,7 +222,7 @@ smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* para
   if (st != SMLA_OK) return st;
   return launch_attend(kernel_layout(*layout), params->n_heads, params->top_k, params->softmax_scale, pool, layer, q,
                        q_pe, topk_idx, block_table, bt_stride, query_start_loc, batch, 0, n_tokens, out, lse,
-                       static_cast<cudaStream_t>(stream), d->err);
+                       static_cast<cudaStream_t>(stream), d->err, nullptr, nullptr, 0, workspace, workspace_bytes);
 }
 
 smla_status_t smla_attend_hisparse(const smla_layout_t* layout, const smla_params_t* params, const void* pool,
@@ -271,6 +278,11 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
   float* scores = static_cast<float*>(workspace);
   int32_t* topk_ws =
       reinterpret_cast<int32_t*>(static_cast<uint8_t*>(workspace) + round_up(static_cast<int64_t>(g) * stride * 4, 256));
+  // the rest of the workspace holds the split-attention partials
+  const size_t used = static_cast<size_t>(round_up(static_cast<int64_t>(g) * stride * 4, 256) +
+                                          round_up(static_cast<int64_t>(g) * params->top_k * 4, 256));
+  void* split_ws = workspace_bytes > used ? static_cast<uint8_t*>(workspace) + used : nullptr;
+  const size_t split_bytes = workspace_bytes > used ? workspace_bytes - used : 0;
   for (int t0 = 0; t0 < n_tokens; t0 += g) {
     const int t1 = t0 + g < n_tokens ? t0 + g : n_tokens;
     int32_t* topk = topk_idx_out ? topk_idx_out + static_cast<int64_t>(t0) * params->top_k : topk_ws;
@@ -280,7 +292,8 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
     st = launch_topk(params->top_k, scores, stride, seq_lens, query_start_loc, batch, t0, t1, topk, s, d->err);
     if (st != SMLA_OK) return st;
     st = launch_attend(L, params->n_heads, params->top_k, params->softmax_scale, pool, layer, q, q_pe, topk,
-                       block_table, bt_stride, query_start_loc, batch, t0, t1, out, lse, s, d->err);
+                       block_table, bt_stride, query_start_loc, batch, t0, t1, out, lse, s, d->err, nullptr, nullptr,
+                       0, split_ws, split_bytes);
     if (st != SMLA_OK) return st;
   }
   return SMLA_OK;

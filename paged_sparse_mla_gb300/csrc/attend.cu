@@ -67,7 +67,8 @@ struct __align__(1024) AttnSmem {
   float m_run[kHeads];
   float alpha[kHeads];
   float l_fin[kHeads];              // 1 / row sum per head
-  int ntiles[2];
+  int ntiles[2];                    // tiles of the unit in each tok slot
+  int tbeg[2];                      // its first tile within the row
   uint64_t tok_full[2], tok_empty[2];
   uint64_t q_full, q_empty;
   uint64_t kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full[2];
@@ -99,6 +100,12 @@ struct AttnArgs {
   // 1: the query tile is loaded by the tensor-memory-access unit (nine 2-D tensor-map copies of
   // 64 heads x 64 dims, 128-byte swizzled as the MMA reads them); 0: by the producer threads
   int q_tma;
+  // Split of each row's tiles into n_splits contiguous ranges (work units u = row * n_splits +
+  // split).  With n_splits > 1 a unit writes its normalised partial output (fp32) and its lse to
+  // part_out [n_splits][n_rows][n_heads][d_latent] and part_lse [n_splits][n_rows][n_heads].
+  int n_splits;
+  float* part_out;
+  float* part_lse;
 };
 
 // Transpose-reduce 32 per-lane values across the 32 lanes of a warp: afterwards
@@ -306,14 +313,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group barrier (what it writes meanwhile is discarded), where the failure is ORed in
     // (bar.red), so that every producer warp leaves the loop together and none is left
     // waiting at a named barrier.
-    for (int tr = blockIdx.x; tr < A.n_rows; tr += gridDim.x, ++n) {
+    const int n_units = A.n_rows * A.n_splits;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
+      const int tr = u / A.n_splits, split = u % A.n_splits;
       const int t = A.tok_begin + tr;
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
-      const int ntiles = row_tiles(idx, A.top_k, lane);
+      const int row_nt = row_tiles(idx, A.top_k, lane);
+      const int tb = split * row_nt / A.n_splits;  // this unit's tiles: [tb, tb + ntiles) of the row
+      const int ntiles = (split + 1) * row_nt / A.n_splits - tb;
       bool fail = *abort != 0;
       if (warp == kFirstProducerWarp && lane == 0 && !fail) {
         if (mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) {
           sm.ntiles[n & 1] = ntiles;
+          sm.tbeg[n & 1] = tb;
           mbar_arrive(&sm.tok_full[n & 1]);
         } else {
           fail = true;
@@ -384,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                L.rec_off + static_cast<int64_t>(j % L.block_size) * L.rec_stride;
       };
       const auto entry = [&](int tile) -> int {
-        const int e = tile * kTile + ptid;
+        const int e = (tb + tile) * kTile + ptid;
         return (ptid < kTile && tile < ntiles && e < A.top_k) ? __ldg(idx + e) : -1;
       };
       const auto block_of = [&](int j) -> int { return j >= 0 ? __ldg(bt + j / L.block_size) : -1; };
@@ -557,7 +569,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&sm.kv_empty[b2]);
       };
-      for (int tr = blockIdx.x; tr < A.n_rows && !*abort; tr += gridDim.x, ++n) {
+      const int n_units = A.n_rows * A.n_splits;
+      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++n) {
         if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
         const int ntiles = sm.ntiles[n & 1];
         mbar_arrive(&sm.tok_empty[n & 1]);
@@ -624,17 +637,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     // As in the producers, a failed wait skips nothing: the thread finishes the tile (what it
     // computes is discarded) and the failure is ORed into the next group barrier, so that the
     // eight warps leave together.
-    for (int tr = blockIdx.x; tr < A.n_rows; tr += gridDim.x, ++n) {
+    const int n_units = A.n_rows * A.n_splits;
+    const bool partial = A.n_splits > 1;
+    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
+      const int tr = u / A.n_splits, split = u % A.n_splits;
       const int t = A.tok_begin + tr;
       const bool go = *abort == 0 && mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort);
       if (bar_red_or(1, kSoftmaxThreads, !go)) break;
       const int ntiles = sm.ntiles[n & 1];
+      const int tb = sm.tbeg[n & 1];
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tok_empty[n & 1]);
+      // destination of this unit: the row's output, or its split's partial
+      const int64_t prow = static_cast<int64_t>(split) * A.n_rows + tr;
+      __nv_bfloat16* out_row = A.out + static_cast<int64_t>(t) * A.n_heads * DL;
+      float* part_row = partial ? A.part_out + prow * A.n_heads * DL : nullptr;
+      float* lse_row = partial ? A.part_lse + prow * A.n_heads : A.lse + static_cast<int64_t>(t) * A.n_heads;
       if (ntiles == 0) {
-        for (int i = tid; i < A.n_heads * DL; i += kSoftmaxThreads)
-          A.out[static_cast<int64_t>(t) * A.n_heads * DL + i] = __float2bfloat16(0.f);
-        if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = -INFINITY;
+        for (int i = tid; i < A.n_heads * DL; i += kSoftmaxThreads) {
+          if (partial) part_row[i] = 0.f;
+          else out_row[i] = __float2bfloat16(0.f);
+        }
+        if (tid < A.n_heads) lse_row[tid] = -INFINITY;
         continue;
       }
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
@@ -644,7 +668,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true, failed = false;
       for (int tile = 0; tile < ntiles; ++tile, ++kk) {
         const int kb = kk & 1;
-        const int e = tile * kTile + key;
+        const int e = (tb + tile) * kTile + key;
         const bool valid = lane < 16 && e < A.top_k && __ldg(idx + e) >= 0;
         ok = ok && mbar_wait(&sm.s_full[kb], (kk >> 1) & 1, A.err, abort);
         tc_fence_after();
@@ -751,7 +775,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (tid < kHeads) {
         const float l = (sm.red[0][tid] + sm.red[1][tid]) + (sm.red[2][tid] + sm.red[3][tid]);
         sm.l_fin[tid] = 1.f / l;  // normalisation as one reciprocal per head
-        if (tid < A.n_heads) A.lse[static_cast<int64_t>(t) * A.n_heads + tid] = (sm.m_run[tid] + log2f(l)) * kLn2;
+        if (tid < A.n_heads) lse_row[tid] = (sm.m_run[tid] + log2f(l)) * kLn2;
       }
       named_bar_sync(1, kSoftmaxThreads);
 #pragma unroll 1
@@ -764,9 +788,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
             const int h = 32 * hh + x;
-            if (h < A.n_heads)
-              A.out[(static_cast<int64_t>(t) * A.n_heads + h) * DL + d] =
-                  __float2bfloat16(__uint_as_float(o[x]) * sm.l_fin[h]);
+            if (h < A.n_heads) {
+              const float v = __uint_as_float(o[x]) * sm.l_fin[h];
+              if (partial) part_row[h * DL + d] = v;
+              else out_row[h * DL + d] = __float2bfloat16(v);
+            }
           }
         }
       }
@@ -782,6 +808,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, 512);
   }
+}
+
+// Merge of a split row's partials: lse = ln sum_s exp(lse_s), out = sum_s exp(lse_s - lse) out_s
+// (fp32, then bf16).  One warp per (token, head); 4 dims per lane per step.
+__global__ void split_merge_kernel(const float* __restrict__ parts, const float* __restrict__ parts_lse,
+                                   int n_splits, int64_t rows, int d, __nv_bfloat16* __restrict__ out,
+                                   float* __restrict__ lse) {
+  const int64_t row = static_cast<int64_t>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= rows) return;
+  float mx = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) mx = fmaxf(mx, __ldg(parts_lse + s * rows + row));
+  float z = 0.f;
+  for (int s = 0; s < n_splits; ++s) {
+    const float l = __ldg(parts_lse + s * rows + row);
+    z += (mx == -INFINITY || l == -INFINITY) ? 0.f : expf(l - mx);
+  }
+  const float inv_z = z > 0.f ? 1.f / z : 0.f;
+  for (int d0 = 4 * lane; d0 < d; d0 += 4 * 32) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < n_splits; ++s) {
+      const float l = __ldg(parts_lse + s * rows + row);
+      if (mx == -INFINITY || l == -INFINITY) continue;
+      const float w = expf(l - mx) * inv_z;
+      const float4 v = __ldg(reinterpret_cast<const float4*>(parts + (s * rows + row) * d + d0));
+      acc.x += w * v.x;
+      acc.y += w * v.y;
+      acc.z += w * v.z;
+      acc.w += w * v.w;
+    }
+    *reinterpret_cast<uint2*>(out + row * d + d0) = make_uint2(pack_bf16x2(acc.x, acc.y), pack_bf16x2(acc.z, acc.w));
+  }
+  if (lane == 0) lse[row] = z > 0.f ? mx + logf(z) : -INFINITY;
 }
 
 template <int NCH, bool WR>
@@ -825,9 +884,19 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       A.q_tma = 1;
   }
-  const int grid = min(A.n_rows, device_sm_count());
+  const int grid = min(A.n_rows * A.n_splits, device_sm_count());
   attend_kernel<NCH, WR><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
-  return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  if (A.n_splits > 1) {
+    const int64_t rows = static_cast<int64_t>(A.n_rows) * A.n_heads;
+    constexpr int kMergeWarps = 8;
+    split_merge_kernel<<<static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, stream>>>(
+        A.part_out, A.part_lse, A.n_splits, rows, (NCH - 1) * 64,
+        A.out + static_cast<int64_t>(A.tok_begin) * A.n_heads * (NCH - 1) * 64,
+        A.lse + static_cast<int64_t>(A.tok_begin) * A.n_heads);
+    if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  }
+  return SMLA_OK;
 }
 
 }  // namespace
@@ -836,9 +905,20 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
                             int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
                             const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
                             int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err,
-                            const void* host_records, const int32_t* host_block_map, int64_t n_host_blocks) {
+                            const void* host_records, const int32_t* host_block_map, int64_t n_host_blocks,
+                            void* split_ws, size_t split_ws_bytes) {
   if (tok_end <= tok_begin) return SMLA_OK;
   if (n_heads > kHeads || L.d_rope > 64 || L.d_latent % 64 != 0) return SMLA_ERR_UNSUPPORTED;
+  // Fewer rows than SMs: each row's tiles are split over up to sms / rows CTAs (one wave of
+  // units), as far as the caller's scratch holds the partials.
+  const int n_rows = tok_end - tok_begin;
+  const int sms = device_sm_count();
+  const int row_tiles_max = (top_k + kTile - 1) / kTile;
+  int n_splits = 1;
+  if (split_ws != nullptr && n_rows < sms && row_tiles_max > 1) {
+    n_splits = min(sms / n_rows, row_tiles_max);
+    while (n_splits > 1 && attend_split_bytes(n_heads, L.d_latent, n_rows * n_splits) > split_ws_bytes) --n_splits;
+  }
   AttnArgs A;
   A.L = L;
   A.n_heads = n_heads;
@@ -861,6 +941,11 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
   A.host_records = static_cast<const uint8_t*>(host_records);
   A.host_block_map = host_block_map;
   A.n_host_blocks = n_host_blocks;
+  A.n_splits = n_splits;
+  A.part_out = n_splits > 1 ? static_cast<float*>(split_ws) : nullptr;
+  A.part_lse = n_splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(split_ws) +
+                                                         split_out_bytes(n_heads, L.d_latent, n_rows * n_splits))
+                            : nullptr;
   switch (L.d_latent / 64) {
     case 1: return launch_nch<2, false>(A, stream);
     case 8: {

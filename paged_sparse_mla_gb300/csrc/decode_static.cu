@@ -89,6 +89,12 @@ extern "C" smla_status_t smla_decode_static(const smla_layout_t* layout, const s
   }
   float* scores = reinterpret_cast<float*>(scratch);
   int32_t* topk_ws = reinterpret_cast<int32_t*>(scratch + round_up_static(g * stride * 4, 256));
+  // what the group leaves of the scratch holds the split-attention partials
+  const int64_t used = round_up_static(g * stride * 4, 256) + round_up_static(g * params->top_k * 4, 256);
+  const size_t split_bytes = static_cast<size_t>(kStaticScratchBytes) > static_cast<size_t>(used)
+                                 ? static_cast<size_t>(kStaticScratchBytes) - static_cast<size_t>(used)
+                                 : 0;
+  void* split_ws = split_bytes > 0 ? scratch + used : nullptr;
   for (int t0 = 0; t0 < n_tokens; t0 += static_cast<int>(g)) {
     const int t1 = t0 + static_cast<int>(g) < n_tokens ? t0 + static_cast<int>(g) : n_tokens;
     int32_t* topk = topk_idx_out ? topk_idx_out + static_cast<int64_t>(t0) * params->top_k : topk_ws;
@@ -98,7 +104,8 @@ extern "C" smla_status_t smla_decode_static(const smla_layout_t* layout, const s
     st = launch_topk(params->top_k, scores, stride, seq_lens, query_start_loc, batch, t0, t1, topk, s, err);
     if (st != SMLA_OK) return st;
     st = launch_attend(L, params->n_heads, params->top_k, params->softmax_scale, pool, layer, q, q_pe, topk,
-                       block_table, bt_stride, query_start_loc, batch, t0, t1, out, lse, s, err);
+                       block_table, bt_stride, query_start_loc, batch, t0, t1, out, lse, s, err, nullptr, nullptr, 0,
+                       split_ws, split_bytes);
     if (st != SMLA_OK) return st;
   }
   return SMLA_OK;

@@ -71,11 +71,23 @@ smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride,
                           const int32_t* query_start_loc, int batch, int tok_begin, int tok_end, int32_t* topk_idx,
                           cudaStream_t stream, unsigned* err);
 
+// Scratch of split attention: fp32 partial outputs [units][n_heads][d_latent] (256-byte rounded),
+// then fp32 partial lse [units][n_heads].
+inline size_t split_out_bytes(int n_heads, int d_latent, int units) {
+  return (static_cast<size_t>(units) * n_heads * d_latent * 4 + 255) / 256 * 256;
+}
+inline size_t attend_split_bytes(int n_heads, int d_latent, int units) {
+  return split_out_bytes(n_heads, d_latent, units) + (static_cast<size_t>(units) * n_heads * 4 + 255) / 256 * 256;
+}
+// Units the fused entry points reserve scratch for (rows x splits never exceed the SM count).
+constexpr int kMaxSplitUnits = 256;
+
+// split_ws / split_ws_bytes: scratch for split attention (nullptr: each row on one CTA).
 smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float softmax_scale, const void* pool,
                             int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
                             const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
                             int tok_begin, int tok_end, void* out, float* lse, cudaStream_t stream, unsigned* err,
                             const void* host_records = nullptr, const int32_t* host_block_map = nullptr,
-                            int64_t n_host_blocks = 0);
+                            int64_t n_host_blocks = 0, void* split_ws = nullptr, size_t split_ws_bytes = 0);
 
 }  // namespace smla

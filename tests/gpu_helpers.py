@@ -44,8 +44,9 @@ def cuda_wl(wl):
     return wl
 
 
-def run_stages(wl, pool, layout, params, layer=0, store=True):
-    """store -> index_scores -> topk -> attend as separate calls; returns host arrays."""
+def run_stages(wl, pool, layout, params, layer=0, store=True, split=True):
+    """store -> index_scores -> topk -> attend as separate calls; returns host arrays.  With `split`
+    the attention gets the scratch the fused step gives it (small batches split tokens over CTAs)."""
     d = wl.dims
     T = wl.n_tokens
     if store:
@@ -59,7 +60,10 @@ def run_stages(wl, pool, layout, params, layer=0, store=True):
     smla.smla_topk(params, scores, wl.seq_lens, wl.query_start_loc, topk)
     out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
-    smla.smla_attend(layout, params, pool, layer, wl.q, wl.q_pe, topk, wl.block_table, wl.query_start_loc, out, lse)
+    nbytes = smla.attend_workspace_size(layout, params, T) if split else 0
+    ws = torch.empty(nbytes, dtype=torch.uint8, device="cuda") if nbytes else None
+    smla.smla_attend(layout, params, pool, layer, wl.q, wl.q_pe, topk, wl.block_table, wl.query_start_loc, out, lse,
+                     workspace=ws)
     err = smla.smla_get_last_error()
     return dict(scores=scores.cpu().numpy(), topk=topk.cpu().numpy(), out=out.float().cpu().numpy(),
                 lse=lse.cpu().numpy(), err=err)
