@@ -284,6 +284,8 @@ def run_gpu(args):
     # the attention's split scratch, as the fused step gives it (small batches split rows over CTAs)
     att_ws_bytes = smla.attend_workspace_size(lay, prm, T)
     att_ws = torch.empty(max(att_ws_bytes, 1), dtype=torch.uint8, device="cuda") if att_ws_bytes else None
+    topk_ws_bytes = smla.topk_workspace_size(prm, T)
+    topk_ws = torch.empty(topk_ws_bytes, dtype=torch.uint8, device="cuda") if topk_ws_bytes else None
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
     for it in range(args.warmup + args.steps):
         # keep the GPU busy while the host enqueues the four launches, so no host gap lands between events
@@ -295,7 +297,7 @@ def run_gpu(args):
         smla.smla_index_scores(lay, prm, pool, 0, wl.q_idx, wl.w, wl.block_table, wl.seq_lens,
                                wl.query_start_loc, wl.max_q, wl.max_ctx, scores, stream=stream)
         ev[2].record(stream)
-        smla.smla_topk(prm, scores, wl.seq_lens, wl.query_start_loc, topk, stream=stream)
+        smla.smla_topk(prm, scores, wl.seq_lens, wl.query_start_loc, topk, stream=stream, workspace=topk_ws)
         ev[3].record(stream)
         smla.smla_attend(lay, prm, pool, 0, wl.q, wl.q_pe, topk, wl.block_table, wl.query_start_loc, out, lse,
                          stream=stream, workspace=att_ws)

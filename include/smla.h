@@ -161,7 +161,14 @@ smla_status_t smla_index_scores(const smla_layout_t* layout, const smla_params_t
  */
 smla_status_t smla_topk(const smla_params_t* params, const float* scores, int64_t scores_stride,
                         const int32_t* seq_lens, const int32_t* query_start_loc, int batch,
-                        int n_tokens, int32_t* topk_idx, void* stream);
+                        int n_tokens, int32_t* topk_idx, void* workspace, size_t workspace_bytes,
+                        void* stream);
+
+/* Scratch bytes with which smla_topk splits long rows of a small batch into segments: each
+ * segment's top-k (positions and scores) becomes a candidate list, then each row's top-k is
+ * taken over its candidates (0 when n_tokens is too large to need it).  workspace may be
+ * NULL (with workspace_bytes 0): every row then runs on one CTA. */
+size_t smla_topk_workspace_size(const smla_params_t* params, int n_tokens);
 
 /*
  * smla_attend -- latent MQA attention over the selected positions.

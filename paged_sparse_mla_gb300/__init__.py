@@ -19,14 +19,14 @@ __all__ = [
     "smla_index_scores", "smla_topk", "smla_attend", "smla_decode", "smla_get_last_error",
     "status_string", "version", "EXPORTED_SYMBOLS", "smla_decode_static", "smla_prefill_chunk",
     "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse", "smla_selftest_wait",
-    "attend_workspace_size",
+    "attend_workspace_size", "topk_workspace_size",
 ]
 
 EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
     "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
-    "smla_selftest_wait", "smla_attend_workspace_size",
+    "smla_selftest_wait", "smla_attend_workspace_size", "smla_topk_workspace_size",
 )
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
@@ -80,7 +80,8 @@ def lib() -> ctypes.CDLL:
             "smla_workspace_size": (ctypes.c_size_t, [LP, PP, _I, _I]),
             "kvpack_store": (_I, [LP, _P, _I, _P, _P, _P, _P, _P, _I, _P]),
             "smla_index_scores": (_I, [LP, PP, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _I64, _P]),
-            "smla_topk": (_I, [PP, _P, _I64, _P, _P, _I, _I, _P, _P]),
+            "smla_topk": (_I, [PP, _P, _I64, _P, _P, _I, _I, _P, _P, ctypes.c_size_t, _P]),
+            "smla_topk_workspace_size": (ctypes.c_size_t, [PP, _I]),
             "smla_attend": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _I, _P, _I, _I, _P, _P, _P, ctypes.c_size_t, _P]),
             "smla_attend_workspace_size": (ctypes.c_size_t, [LP, PP, _I]),
             "smla_decode": (_I, [LP, PP, _P, _I, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _P, _P, _I, _I,
@@ -179,12 +180,19 @@ def smla_index_scores(layout, params, pool, layer, q_idx, w, block_table, seq_le
                                    scores.stride(0), _stream(stream)), "smla_index_scores")
 
 
-def smla_topk(params, scores, seq_lens, query_start_loc, topk_idx, stream=None):
+def topk_workspace_size(params, n_tokens) -> int:
+    return int(lib().smla_topk_workspace_size(ctypes.byref(params), n_tokens))
+
+
+def smla_topk(params, scores, seq_lens, query_start_loc, topk_idx, stream=None, workspace=None):
+    """Exact top-k per row.  `workspace` (uint8 device tensor of at least topk_workspace_size(...)
+    bytes, optional) lets a small batch of long rows split each row over CTAs."""
     _expect(scores, torch.float32, "scores")
     _expect(topk_idx, torch.int32, "topk_idx")
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().smla_topk(ctypes.byref(params), _ptr(scores), scores.stride(0), _ptr(seq_lens),
                            _ptr(query_start_loc), seq_lens.numel(), topk_idx.shape[0], _ptr(topk_idx),
-                           _stream(stream)), "smla_topk")
+                           _ptr(workspace), ws_bytes, _stream(stream)), "smla_topk")
 
 
 def attend_workspace_size(layout, params, n_tokens) -> int:

@@ -1,5 +1,6 @@
 // C ABI of libsmla: argument checks, workspace sizing, the fused step, and the
 // latched device error word.  Every entry point is declared in include/smla.h.
+#include <algorithm>
 #include <cstring>
 
 #include "smla_internal.h"
@@ -149,9 +150,12 @@ size_t smla_workspace_size(const smla_layout_t* layout, const smla_params_t* par
   if (!layout_ok(layout) || params == nullptr || n_tokens <= 0 || max_ctx <= 0 || params->top_k <= 0) return 0;
   const int64_t stride = round_up(max_ctx, 4);
   const int g = query_group(n_tokens, stride);
+  // the split top-k's candidates and the split attention's partials share one region (the stream
+  // runs them one after the other)
+  const size_t split = std::max(smla_attend_workspace_size(layout, params, g), smla_topk_workspace_size(params, g));
   return static_cast<size_t>(round_up(static_cast<int64_t>(g) * stride * 4, 256) +
                              round_up(static_cast<int64_t>(g) * params->top_k * 4, 256)) +
-         smla_attend_workspace_size(layout, params, g);
+         split;
 }
 
 size_t smla_attend_workspace_size(const smla_layout_t* layout, const smla_params_t* params, int n_tokens) {
@@ -195,15 +199,23 @@ smla_status_t smla_index_scores(const smla_layout_t* layout, const smla_params_t
 
 smla_status_t smla_topk(const smla_params_t* params, const float* scores, int64_t scores_stride,
                         const int32_t* seq_lens, const int32_t* query_start_loc, int batch, int n_tokens,
-                        int32_t* topk_idx, void* stream) {
-  if (!params || params->top_k <= 0 || batch <= 0 || n_tokens < 0 || scores_stride <= 0) return SMLA_ERR_INVALID_ARG;
+                        int32_t* topk_idx, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!params || params->top_k <= 0 || batch <= 0 || n_tokens < 0 || scores_stride <= 0 ||
+      (workspace == nullptr && workspace_bytes != 0))
+    return SMLA_ERR_INVALID_ARG;
   if (n_tokens == 0) return SMLA_OK;
   if (!scores || !seq_lens || !query_start_loc || !topk_idx) return SMLA_ERR_INVALID_ARG;
   DeviceInfo* d;
   smla_status_t st = check_device(&d);
   if (st != SMLA_OK) return st;
   return launch_topk(params->top_k, scores, scores_stride, seq_lens, query_start_loc, batch, 0, n_tokens, topk_idx,
-                     static_cast<cudaStream_t>(stream), d->err);
+                     static_cast<cudaStream_t>(stream), d->err, workspace, workspace_bytes);
+}
+
+size_t smla_topk_workspace_size(const smla_params_t* params, int n_tokens) {
+  if (params == nullptr || params->top_k <= 0 || n_tokens <= 0) return 0;
+  // rows fewer than a wave of top-k CTAs are split; rows x segments stay within kMaxTopkSplitRows
+  return n_tokens < kMaxTopkSplitRows ? topk_split_bytes(kMaxTopkSplitRows, params->top_k) : 0;
 }
 
 smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* params, const void* pool, int layer,
@@ -289,7 +301,8 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
     st = launch_index_scores(L, params->n_idx_heads, pool, layer, q_idx, w, block_table, bt_stride, seq_lens,
                              query_start_loc, batch, t0, t1, max_q, max_ctx, scores, stride, s, d->err);
     if (st != SMLA_OK) return st;
-    st = launch_topk(params->top_k, scores, stride, seq_lens, query_start_loc, batch, t0, t1, topk, s, d->err);
+    st = launch_topk(params->top_k, scores, stride, seq_lens, query_start_loc, batch, t0, t1, topk, s, d->err,
+                     split_ws, split_bytes);
     if (st != SMLA_OK) return st;
     st = launch_attend(L, params->n_heads, params->top_k, params->softmax_scale, pool, layer, q, q_pe, topk,
                        block_table, bt_stride, query_start_loc, batch, t0, t1, out, lse, s, d->err, nullptr, nullptr,

@@ -101,7 +101,8 @@ extern "C" smla_status_t smla_decode_static(const smla_layout_t* layout, const s
     st = launch_index_scores(L, params->n_idx_heads, pool, layer, q_idx, w, block_table, bt_stride, seq_lens,
                              query_start_loc, batch, t0, t1, max_q, max_ctx, scores, stride, s, err);
     if (st != SMLA_OK) return st;
-    st = launch_topk(params->top_k, scores, stride, seq_lens, query_start_loc, batch, t0, t1, topk, s, err);
+    st = launch_topk(params->top_k, scores, stride, seq_lens, query_start_loc, batch, t0, t1, topk, s, err, split_ws,
+                     split_bytes);
     if (st != SMLA_OK) return st;
     st = launch_attend(L, params->n_heads, params->top_k, params->softmax_scale, pool, layer, q, q_pe, topk,
                        block_table, bt_stride, query_start_loc, batch, t0, t1, out, lse, s, err, nullptr, nullptr, 0,

@@ -67,9 +67,18 @@ inline int64_t wave_aligned_group(int64_t g, int n_tokens) {
   return (wave > 0 && g >= wave) ? g - g % wave : g;
 }
 
+// Scratch of the split top-k: candidate positions, then candidate scores, for `seg_rows`
+// (row, segment) pairs of k entries each (two 256-byte rounded halves).
+inline size_t topk_split_bytes(int seg_rows, int k) {
+  return 2 * ((static_cast<size_t>(seg_rows) * k * 4 + 255) / 256 * 256);
+}
+// (row, segment) pairs the split top-k may use (any wave of top-k CTAs fits).
+constexpr int kMaxTopkSplitRows = 512;
+
+// split_ws / split_ws_bytes: scratch for splitting rows into segments (nullptr: one CTA per row).
 smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
                           const int32_t* query_start_loc, int batch, int tok_begin, int tok_end, int32_t* topk_idx,
-                          cudaStream_t stream, unsigned* err);
+                          cudaStream_t stream, unsigned* err, void* split_ws = nullptr, size_t split_ws_bytes = 0);
 
 // Scratch of split attention: fp32 partial outputs [units][n_heads][d_latent] (256-byte rounded),
 // then fp32 partial lse [units][n_heads].

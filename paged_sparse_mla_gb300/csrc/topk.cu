@@ -45,6 +45,11 @@ struct TopkSmem {
   int warp_tot[32];
   int sel_bin, sel_above;
   int wcnt[kWarps], wgt[kWarps], weq[kWarps];  // per-warp candidate lists: length, > T, == T
+  // where the row's selection goes besides the output row (see RowOut), kept here rather than in
+  // registers, which the collection pass needs
+  int pos_base;
+  const int32_t* map;
+  float* score_out;
 };
 
 __device__ __forceinline__ uint32_t order_key(float x) {
@@ -212,6 +217,28 @@ __device__ uint32_t radix_select_lists(TopkSmem& sm, int k, int& rem, uint32_t& 
   return prefix;
 }
 
+// Output slot i of the row (o) receives position j.  kPlain: as j.  Otherwise as
+// sm.pos_base + j (or sm.map[j]), and sm.score_out[i] receives the score s[j] when it is set;
+// only `o` travels in registers.
+template <bool kPlain>
+__device__ __forceinline__ void emit(const TopkSmem& sm, int32_t* o, const float* s, int i, int j) {
+  if constexpr (kPlain) {
+    o[i] = j;
+  } else {
+    const int32_t* map = sm.map;
+    o[i] = map ? __ldg(map + j) : sm.pos_base + j;
+    if (float* so = sm.score_out) so[i] = __ldg(s + j);
+  }
+}
+template <bool kPlain>
+__device__ __forceinline__ void emit_pad(const TopkSmem& sm, int32_t* o, int i) {
+  o[i] = -1;
+  if constexpr (!kPlain) {
+    if (float* so = sm.score_out) so[i] = -INFINITY;
+  }
+}
+
+template <bool kPlain>
 __device__ void topk_slow(TopkSmem& sm, const float* s, int n, int k, int32_t* o) {
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
@@ -254,27 +281,29 @@ __device__ void topk_slow(TopkSmem& sm, const float* s, int n, int k, int32_t* o
       keep = eq_seen < eq_take;
       ++eq_seen;
     }
-    if (keep) o[pos++] = j;
+    if (keep) emit<kPlain>(sm, o, s, pos++, j);
   }
 }
 
-// The top-k of one row (every thread of the CTA; each branch below is CTA-uniform).
-__device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__ scores, int64_t stride,
-                         const int32_t* __restrict__ seq_lens, const int32_t* __restrict__ qsl, int batch,
-                         int tok_begin, int32_t* __restrict__ out) {
-  const int t = tok_begin + row;
+// Positions visible to query token t (0..p).
+__device__ __forceinline__ int visible(const int32_t* seq_lens, const int32_t* qsl, int batch, int t) {
   const int b = seq_of_token(qsl, batch, t);
   const int q0 = __ldg(qsl + b), n_q = __ldg(qsl + b + 1) - q0;
-  const int n = __ldg(seq_lens + b) - n_q + (t - q0) + 1;  // positions 0..p
-  const float* s = scores + static_cast<int64_t>(row) * stride;
-  int32_t* o = out + static_cast<int64_t>(row) * k;
+  return __ldg(seq_lens + b) - n_q + (t - q0) + 1;
+}
 
+// The top-k of the n scores s[0..n) (every thread of the CTA; each branch below is CTA-uniform).
+template <bool kPlain>
+__device__ void topk_core(TopkSmem& sm, const float* __restrict__ s, int n, int k, int32_t* o) {
   if (n <= k) {
-    for (int i = threadIdx.x; i < k; i += kThreads) o[i] = i < n ? i : -1;
+    for (int i = threadIdx.x; i < k; i += kThreads) {
+      if (i < n) emit<kPlain>(sm, o, s, i, i);
+      else emit_pad<kPlain>(sm, o, i);
+    }
     return;
   }
   if (k > kMaxK) {
-    topk_slow(sm, s, n, k, o);
+    topk_slow<kPlain>(sm, s, n, k, o);
     return;
   }
   // Segment of warp w in the collection pass below.
@@ -306,7 +335,7 @@ __device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__
     thr = radix_select(sm, samp, kSample, want, rem, 2);  // 24 bits: the threshold's bin is kept whole
   }
   if (!aligned) {  // rows that are not 16-byte aligned
-    topk_slow(sm, s, n, k, o);
+    topk_slow<kPlain>(sm, s, n, k, o);
     return;
   }
   // ---- one pass: warp w scans its own contiguous segment and appends every key >= thr, in
@@ -379,7 +408,7 @@ __device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__
     over |= sm.wcnt[w] > kWarpCap;
   }
   if (n_cand < k || over) {  // the sample's guess missed: exact radix select over the row
-    topk_slow(sm, s, n, k, o);
+    topk_slow<kPlain>(sm, s, n, k, o);
     return;
   }
   // ---- exact k-th largest key T among the candidates ----
@@ -428,7 +457,7 @@ __device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__
     const uint32_t below = (1u << lane) - 1u;
     const bool keep = j < count && (key > T || (is_eq && ties_seen + __popc(eq_mask & below) < take_eq));
     const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
-    if (keep) o[out_off + written + __popc(keep_mask & below)] = pos;
+    if (keep) emit<kPlain>(sm, o, s, out_off + written + __popc(keep_mask & below), pos);
     written += __popc(keep_mask);
     ties_seen += __popc(eq_mask);
   }
@@ -439,16 +468,65 @@ __device__ void topk_row(TopkSmem& sm, int row, int k, const float* __restrict__
 // pass over G rows runs in the opposite direction to the one before, so a CTA pairs a
 // front row with a back row.  In causal prefill, where a row's length grows with its
 // position, this evens the CTAs' work in the manner of front/back context pairing.
-__global__ void __launch_bounds__(kThreads) topk_kernel(int k, const float* __restrict__ scores, int64_t stride,
+//
+// Rows longer than the batch can fill the GPU with are split (stage 1 and 2): stage 1 takes the
+// n_seg contiguous segments of every row as rows of their own and writes each segment's top-k
+// (positions and scores) as candidates; stage 2 selects the top-k of each row's n_seg * k
+// candidates.  A position of the row's top-k is in its segment's top-k (at most k - 1 positions
+// of the segment rank above it), so the candidates hold the answer; they are laid out in segment
+// order with ascending positions inside, so candidate order is position order and stage 2's ties
+// (lower index) and ascending output are the row's.
+template <bool kPlain>
+__global__ void __launch_bounds__(kThreads, 2) topk_kernel(int k, const float* __restrict__ scores, int64_t stride,
                                                         const int32_t* __restrict__ seq_lens,
                                                         const int32_t* __restrict__ qsl, int batch, int tok_begin,
-                                                        int n_rows, int32_t* __restrict__ out) {
+                                                        int n_rows, int32_t* __restrict__ out, int stage, int n_seg,
+                                                        int32_t* __restrict__ cand_pos,
+                                                        float* __restrict__ cand_score) {
   extern __shared__ uint8_t smem_raw[];
   TopkSmem& sm = *reinterpret_cast<TopkSmem*>(smem_raw);
   const int G = static_cast<int>(gridDim.x);
   for (int base = 0, pass = 0; base < n_rows; base += G, ++pass) {
     const int row = base + ((pass & 1) ? G - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
-    if (row < n_rows) topk_row(sm, row, k, scores, stride, seq_lens, qsl, batch, tok_begin, out);
+    if constexpr (kPlain) {  // one row per CTA pass, positions written as they are
+      if (row < n_rows)
+        topk_core<true>(sm, scores + static_cast<int64_t>(row) * stride,
+                        visible(seq_lens, qsl, batch, tok_begin + row), k, out + static_cast<int64_t>(row) * k);
+    } else if (row < n_rows) {
+      const float* s;
+      int n;
+      int32_t* o = out + static_cast<int64_t>(row) * k;
+      int pos_base = 0;
+      const int32_t* map = nullptr;
+      float* score_out = nullptr;
+      if (stage == 2) {
+        const int64_t c0 = static_cast<int64_t>(row) * n_seg * k;
+        s = cand_score + c0;
+        n = n_seg * k;
+        map = cand_pos + c0;
+      } else {
+        const int tr = stage == 1 ? row / n_seg : row;
+        n = visible(seq_lens, qsl, batch, tok_begin + tr);
+        s = scores + static_cast<int64_t>(tr) * stride;
+        if (stage == 1) {
+          const int len = ((n + n_seg - 1) / n_seg + 3) & ~3;  // 16-byte aligned segment starts
+          const int lo = min(n, (row % n_seg) * len), hi = min(n, lo + len);
+          const int64_t c0 = static_cast<int64_t>(row) * k;
+          s += lo;
+          n = hi - lo;
+          o = cand_pos + c0;
+          pos_base = lo;
+          score_out = cand_score + c0;
+        }
+      }
+      if (threadIdx.x == 0) {
+        sm.pos_base = pos_base;
+        sm.map = map;
+        sm.score_out = score_out;
+      }
+      __syncthreads();
+      topk_core<false>(sm, s, n, k, o);
+    }
     __syncthreads();  // shared memory is reused by the next row
   }
 }
@@ -463,11 +541,13 @@ int topk_wave() {
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
   if (wave[dev] == 0) {
     const size_t smem = sizeof(TopkSmem);
-    if (cudaFuncSetAttribute(topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
-        cudaSuccess)
+    if (cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess ||
+        cudaFuncSetAttribute(topk_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
+            cudaSuccess)
       return 0;
     int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel, kThreads, smem) != cudaSuccess ||
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true>, kThreads, smem) != cudaSuccess ||
         per_sm <= 0)
       return 0;
     wave[dev] = per_sm * device_sm_count();
@@ -477,15 +557,40 @@ int topk_wave() {
 
 smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
                           const int32_t* query_start_loc, int batch, int tok_begin, int tok_end, int32_t* topk_idx,
-                          cudaStream_t stream, unsigned* err) {
+                          cudaStream_t stream, unsigned* err, void* split_ws, size_t split_ws_bytes) {
   (void)err;
   const int rows = tok_end - tok_begin;
   if (rows <= 0) return SMLA_OK;
   const int wave = topk_wave();
   if (wave <= 0) return SMLA_ERR_CUDA;
+  // Fewer rows than a wave of CTAs, and rows long against k: split each row into n_seg segments
+  // (stage 1, rows x n_seg CTAs) and merge their candidates (stage 2).  A pass costs a fixed
+  // ~23 us (sample, selections) plus its positions, so two passes over n / n_seg and n_seg * k
+  // positions beat one over n only for rows of more than ~64k positions; n_seg ~ sqrt(n / k)
+  // balances the two passes.
+  int n_seg = 1;
+  if (split_ws != nullptr && rows < wave && top_k <= kMaxK && scores_stride >= 64 * static_cast<int64_t>(top_k)) {
+    int by_len = 1;
+    while (static_cast<int64_t>(by_len + 1) * (by_len + 1) * top_k <= scores_stride) ++by_len;
+    n_seg = min(min(wave / rows, by_len), kMaxTopkSplitRows / rows);
+    while (n_seg > 1 && topk_split_bytes(rows * n_seg, top_k) > split_ws_bytes) --n_seg;
+  }
+  if (n_seg >= 2) {
+    const int seg_rows = rows * n_seg;
+    int32_t* cand_pos = static_cast<int32_t*>(split_ws);
+    float* cand_score = reinterpret_cast<float*>(static_cast<uint8_t*>(split_ws) + topk_split_bytes(seg_rows, top_k) / 2);
+    topk_kernel<false><<<min(seg_rows, wave), kThreads, sizeof(TopkSmem), stream>>>(
+        top_k, scores, scores_stride, seq_lens, query_start_loc, batch, tok_begin, seg_rows, topk_idx, 1, n_seg,
+        cand_pos, cand_score);
+    if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+    topk_kernel<false><<<rows, kThreads, sizeof(TopkSmem), stream>>>(top_k, scores, scores_stride, seq_lens,
+                                                              query_start_loc, batch, tok_begin, rows, topk_idx, 2,
+                                                              n_seg, cand_pos, cand_score);
+    return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
+  }
   const int grid = rows < wave ? rows : wave;
-  topk_kernel<<<grid, kThreads, sizeof(TopkSmem), stream>>>(top_k, scores, scores_stride, seq_lens, query_start_loc,
-                                                             batch, tok_begin, rows, topk_idx);
+  topk_kernel<true><<<grid, kThreads, sizeof(TopkSmem), stream>>>(top_k, scores, scores_stride, seq_lens, query_start_loc,
+                                                             batch, tok_begin, rows, topk_idx, 0, 1, nullptr, nullptr);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 

@@ -57,7 +57,9 @@ def run_stages(wl, pool, layout, params, layer=0, store=True, split=True):
     smla.smla_index_scores(layout, params, pool, layer, wl.q_idx, wl.w, wl.block_table, wl.seq_lens,
                            wl.query_start_loc, wl.max_q, wl.max_ctx, scores)
     topk = torch.empty((T, params.top_k), dtype=torch.int32, device="cuda")
-    smla.smla_topk(params, scores, wl.seq_lens, wl.query_start_loc, topk)
+    tbytes = smla.topk_workspace_size(params, T) if split else 0
+    tws = torch.empty(tbytes, dtype=torch.uint8, device="cuda") if tbytes else None
+    smla.smla_topk(params, scores, wl.seq_lens, wl.query_start_loc, topk, workspace=tws)
     out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
     nbytes = smla.attend_workspace_size(layout, params, T) if split else 0

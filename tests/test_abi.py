@@ -60,7 +60,9 @@ def test_host_side_argument_checks(lib):
     assert lib.kvpack_store(L, None, 0, None, None, None, None, None, 1, None) == 1
     assert lib.kvpack_store(L, None, 0, None, None, None, None, None, 0, None) == 0   # nothing to do
     assert lib.kvpack_store(L, ctypes.c_void_p(256), 5, None, None, None, None, None, 1, None) == 1  # bad layer
-    assert lib.smla_topk(P, None, 0, None, None, 1, 4, None, None) == 1
+    assert lib.smla_topk(P, None, 0, None, None, 1, 4, None, None, 0, None) == 1
+    assert lib.smla_topk_workspace_size(P, 4) > 0               # few rows: the segment scratch
+    assert lib.smla_topk_workspace_size(P, 100000) == 0         # many rows: no split
     assert lib.smla_attend(L, P, None, 0, None, None, None, None, 0, None, 1, 3, None, None, None, 0, None) == 1
     # a workspace size without a workspace is an argument error
     assert lib.smla_attend(L, P, None, 0, None, None, None, None, 0, None, 1, 0, None, None, None, 64, None) == 1

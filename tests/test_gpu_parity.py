@@ -253,6 +253,27 @@ def test_split_attention_matches_oracle_and_one_cta_path(lens):
     assert np.abs(o - res["out"]).max() <= 1e-2
 
 
+@pytest.mark.parametrize("lens", [[140000, 61000, 30000, 9000], [300000], [200000, 150000, 5000, 1, 3000]])
+def test_topk_rows_split_into_segments(lens):
+    """Few long rows and a scratch: each row's segments are selected on their own CTAs and the
+    candidates merged.  Heavy ties (across segment boundaries too): every row equals the oracle's."""
+    rng = np.random.default_rng(97 + len(lens))
+    R, L, k = len(lens), max(lens), 2048
+    stride = (L + 3) // 4 * 4
+    scores = rng.integers(-60, 61, size=(R, stride)).astype(np.float32) * np.float32(0.25)
+    seq_lens = torch.tensor(lens, dtype=torch.int32, device="cuda")
+    qsl = torch.arange(R + 1, dtype=torch.int32, device="cuda")
+    prm = smla.make_params(64, 64, k, 1.0)
+    ws = torch.empty(smla.topk_workspace_size(prm, R), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    out = torch.full((R, k), -7, dtype=torch.int32, device="cuda")
+    smla.smla_topk(prm, torch.as_tensor(scores, device="cuda"), seq_lens, qsl, out, workspace=ws)
+    assert smla.smla_get_last_error() == 0
+    got = out.cpu().numpy()
+    for t in range(R):
+        assert np.array_equal(got[t], oracle.topk_select(scores[t, :lens[t]], k)), f"row {t}"
+
+
 def test_topk_more_rows_than_one_wave():
     """1,000 causal rows of one sequence: the top-k grid is one resident wave and each CTA takes
     a front row and a back row in alternate passes; every row must still equal the oracle's."""
