@@ -257,7 +257,7 @@ __device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
   return (last + kTile) / kTile;
 }
 
-template <int NCH, bool WR>
+template <int NCH, bool WR, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const AttnArgs A, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap qpe_map) {
@@ -313,19 +313,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group barrier (what it writes meanwhile is discarded), where the failure is ORed in
     // (bar.red), so that every producer warp leaves the loop together and none is left
     // waiting at a named barrier.
-    const int n_units = A.n_rows * A.n_splits;
+    const int n_splits = SPLIT ? A.n_splits : 1;  // compile-time 1 without the split
+    const int n_units = A.n_rows * n_splits;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
-      const int tr = u / A.n_splits, split = u % A.n_splits;
+      const int tr = u / n_splits, split = u % n_splits;
       const int t = A.tok_begin + tr;
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
       const int row_nt = row_tiles(idx, A.top_k, lane);
-      const int tb = split * row_nt / A.n_splits;  // this unit's tiles: [tb, tb + ntiles) of the row
-      const int ntiles = (split + 1) * row_nt / A.n_splits - tb;
+      const int tb = split * row_nt / n_splits;  // this unit's tiles: [tb, tb + ntiles) of the row
+      const int ntiles = (split + 1) * row_nt / n_splits - tb;
       bool fail = *abort != 0;
       if (warp == kFirstProducerWarp && lane == 0 && !fail) {
         if (mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) {
           sm.ntiles[n & 1] = ntiles;
-          sm.tbeg[n & 1] = tb;
+          if (SPLIT) sm.tbeg[n & 1] = tb;
           mbar_arrive(&sm.tok_full[n & 1]);
         } else {
           fail = true;
@@ -569,7 +570,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&sm.kv_empty[b2]);
       };
-      const int n_units = A.n_rows * A.n_splits;
+      const int n_units = A.n_rows * (SPLIT ? A.n_splits : 1);
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++n) {
         if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
         const int ntiles = sm.ntiles[n & 1];
@@ -637,15 +638,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     // As in the producers, a failed wait skips nothing: the thread finishes the tile (what it
     // computes is discarded) and the failure is ORed into the next group barrier, so that the
     // eight warps leave together.
-    const int n_units = A.n_rows * A.n_splits;
-    const bool partial = A.n_splits > 1;
+    const int n_splits = SPLIT ? A.n_splits : 1;
+    const int n_units = A.n_rows * n_splits;
+    constexpr bool partial = SPLIT;
     for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
-      const int tr = u / A.n_splits, split = u % A.n_splits;
+      const int tr = u / n_splits, split = u % n_splits;
       const int t = A.tok_begin + tr;
       const bool go = *abort == 0 && mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort);
       if (bar_red_or(1, kSoftmaxThreads, !go)) break;
       const int ntiles = sm.ntiles[n & 1];
-      const int tb = sm.tbeg[n & 1];
+      const int tb = SPLIT ? sm.tbeg[n & 1] : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tok_empty[n & 1]);
       // destination of this unit: the row's output, or its split's partial
@@ -784,15 +786,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t o[32];
         tmem_ld32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
         tmem_ld_wait(o);
-        if (d < DL) {
+        if (d < DL && !partial) {
 #pragma unroll
           for (int x = 0; x < 32; ++x) {
             const int h = 32 * hh + x;
-            if (h < A.n_heads) {
-              const float v = __uint_as_float(o[x]) * sm.l_fin[h];
-              if (partial) part_row[h * DL + d] = v;
-              else out_row[h * DL + d] = __float2bfloat16(v);
-            }
+            if (h < A.n_heads) out_row[h * DL + d] = __float2bfloat16(__uint_as_float(o[x]) * sm.l_fin[h]);
+          }
+        } else if (d < DL) {
+#pragma unroll
+          for (int x = 0; x < 32; ++x) {
+            const int h = 32 * hh + x;
+            if (h < A.n_heads) part_row[h * DL + d] = __uint_as_float(o[x]) * sm.l_fin[h];
           }
         }
       }
@@ -848,14 +852,19 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem<NCH>) + 1024;
   static bool attr_set = false;
   if (!attr_set) {
-    if (cudaFuncSetAttribute(attend_kernel<NCH, WR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attend_kernel<NCH, WR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(attend_kernel<NCH, WR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     // setmaxnreg.inc can only draw on the registers the CTA was launched with;
     // refuse to launch if the compiled allocation does not cover the split.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH, WR>) != cudaSuccess) return SMLA_ERR_CUDA;
-    if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
+    cudaFuncAttributes fs;
+    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH, WR, false>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fs, attend_kernel<NCH, WR, true>) != cudaSuccess)
+      return SMLA_ERR_CUDA;
+    if (fa.numRegs < kLaunchRegs || fs.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set = true;
   }
   // Query tiles by tensor-map copies when they match the shared-memory tile exactly: 64 heads,
@@ -885,7 +894,10 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
       A.q_tma = 1;
   }
   const int grid = min(A.n_rows * A.n_splits, device_sm_count());
-  attend_kernel<NCH, WR><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
+  if (A.n_splits > 1)
+    attend_kernel<NCH, WR, true><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
+  else
+    attend_kernel<NCH, WR, false><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
   if (A.n_splits > 1) {
     const int64_t rows = static_cast<int64_t>(A.n_rows) * A.n_heads;
