@@ -36,7 +36,9 @@
  *     word and reported by smla_get_last_error(); the offending read is
  *     clamped or skipped, never performed out of bounds.
  *   - No C++ exceptions cross the ABI.  Calls on different streams may run
- *     concurrently; the latched error word is shared by all of them.
+ *     concurrently; the latched error word is shared by all of them.  Calls
+ *     may come from several host threads: the library's once-per-device
+ *     set-up (device attributes, symbol addresses) is synchronised.
  *
  * Query geometry shared by the calls: sequence b has seq_lens[b] cached
  * tokens INCLUDING this step's tokens, and its query tokens are rows

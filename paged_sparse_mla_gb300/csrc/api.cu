@@ -1,7 +1,9 @@
 // C ABI of libsmla: argument checks, workspace sizing, the fused step, and the
 // latched device error word.  Every entry point is declared in include/smla.h.
 #include <algorithm>
+#include <atomic>
 #include <cstring>
+#include <mutex>
 
 #include "smla_internal.h"
 
@@ -38,18 +40,23 @@ __global__ void wait_selftest_kernel(unsigned* err, uint64_t limit_ns) {
 }
 
 struct DeviceInfo {
-  bool init = false;
+  std::atomic<bool> init{false};  // set (release) once the fields below are filled in
   int sms = 0;
   bool supported = false;
   unsigned* err = nullptr;
 };
 DeviceInfo g_dev[kMaxDevices];
+std::mutex g_dev_mutex;  // serialises the one-time set-up of a device's entry
 
+// The calling thread's current device, its attributes and the device address of
+// the error word; filled in once per device, safely when host threads race to it.
 DeviceInfo* current_device() {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
   DeviceInfo& d = g_dev[dev];
-  if (!d.init) {
+  if (d.init.load(std::memory_order_acquire)) return &d;
+  std::lock_guard<std::mutex> lock(g_dev_mutex);
+  if (!d.init.load(std::memory_order_relaxed)) {
     int major = 0, minor = 0;
     cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev);
@@ -58,7 +65,7 @@ DeviceInfo* current_device() {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
     d.err = static_cast<unsigned*>(p);
-    d.init = true;
+    d.init.store(true, std::memory_order_release);
   }
   return &d;
 }

@@ -20,6 +20,8 @@
 // for every position the top-k reads, and every top-k row is written in full.
 // Calls whose kernels overlap on the GPU (different streams without ordering
 // between them) race on the array; order them on one stream.
+#include <atomic>
+
 #include "smla_internal.h"
 
 namespace smla {
@@ -30,7 +32,10 @@ constexpr int kMaxDevicesStatic = 64;
 
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 
-uint8_t* g_static_scratch_addr[kMaxDevicesStatic] = {};
+// Device address of the array per device (nullptr until the first call there).  Racing
+// first calls from several host threads all look up the same address; the atomic store
+// publishes it to the others.
+std::atomic<uint8_t*> g_static_scratch_addr[kMaxDevicesStatic] = {};
 
 inline int64_t round_up_static(int64_t x, int64_t m) { return (x + m - 1) / m * m; }
 
@@ -38,12 +43,14 @@ inline int64_t round_up_static(int64_t x, int64_t m) { return (x + m - 1) / m * 
 smla_status_t static_scratch(uint8_t** out) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevicesStatic) return SMLA_ERR_CUDA;
-  if (g_static_scratch_addr[dev] == nullptr) {
+  uint8_t* addr = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+  if (addr == nullptr) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_static_scratch) != cudaSuccess) return SMLA_ERR_CUDA;
-    g_static_scratch_addr[dev] = static_cast<uint8_t*>(p);
+    addr = static_cast<uint8_t*>(p);
+    g_static_scratch_addr[dev].store(addr, std::memory_order_release);
   }
-  *out = g_static_scratch_addr[dev];
+  *out = addr;
   return SMLA_OK;
 }
 
