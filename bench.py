@@ -398,7 +398,8 @@ def run_gpu(args):
         t_ten = a["flops"] / (fpk * 1e12) if fpk else 0.0
         wname = wl.name
         tr = tt.get((dominant, wname))
-        traffic = tr[1] if tr is not None and tr[0] == source_sha(dominant) else None
+        # the recorded bytes are for the full-size workload of that name and the kernel source hashed
+        traffic = tr[1] if tr is not None and tr[0] == source_sha(dominant) and args.scale == 1.0 else None
         if t_ten > t_hbm:
             ach = a["flops"] / (msk / 1e3) / 1e12
             roof = {"kernel": dominant, "bound": "tensor", "achieved": round(ach, 1), "peak": round(fpk, 1),
@@ -424,7 +425,7 @@ def run_gpu(args):
                    "top_k": d.top_k, "heads": d.n_heads, "idx_heads": d.n_idx_heads, "block_size": d.block_size,
                    "pool_gb": round(lay.pool_bytes / 1e9, 3), "parallelism": f"replicas x{world}",
                    "l2": f"inputs larger than L2: {step_b / 1e6:.0f} MB unique per step > 129 MB",
-                   "query_groups_per_step": n_groups},
+                   "query_groups_per_step": n_groups, "context_scale": args.scale},
         "hbm_gbs": round(step_b / (ms_step / 1e3) / 1e9, 1),
         "hbm_frac": round(step_b / (ms_step / 1e3) / 1e9 / pk["hbm"], 4),
         "step_bytes": {"unique": step_b, "logical": acct["_step"]["logical_bytes"]},

@@ -93,6 +93,12 @@ int query_group(int n_tokens, int64_t stride) {
 
 }  // namespace
 
+int current_device_index() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDeviceSlots) return -1;
+  return dev;
+}
+
 unsigned* device_error_word() {
   DeviceInfo* d = current_device();
   return d ? d->err : nullptr;

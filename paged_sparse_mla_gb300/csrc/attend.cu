@@ -850,8 +850,10 @@ __global__ void split_merge_kernel(const float* __restrict__ parts, const float*
 template <int NCH, bool WR>
 smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem<NCH>) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<bool> attr_set[kMaxDeviceSlots] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return SMLA_ERR_CUDA;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(attend_kernel<NCH, WR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
         cudaFuncSetAttribute(attend_kernel<NCH, WR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -865,7 +867,7 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
         cudaFuncGetAttributes(&fs, attend_kernel<NCH, WR, true>) != cudaSuccess)
       return SMLA_ERR_CUDA;
     if (fa.numRegs < kLaunchRegs || fs.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
-    attr_set = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   // Query tiles by tensor-map copies when they match the shared-memory tile exactly: 64 heads,
   // 64-dim chunks (the latent in NCH - 1 of them, the rope in one), 16-byte aligned rows.

@@ -265,12 +265,14 @@ smla_status_t smla_dcp_topk_merge(const float* shard_scores, int64_t shard_strid
   if (static_cast<int64_t>(n_shards) * top_k > kMaxCand) return SMLA_ERR_UNSUPPORTED;
   if (n_shards > 64) return SMLA_ERR_UNSUPPORTED;
   const size_t smem = sizeof(MergeSmem);
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<bool> attr_set[kMaxDeviceSlots] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return SMLA_ERR_CUDA;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
         cudaSuccess)
       return SMLA_ERR_UNSUPPORTED;
-    attr_set = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   topk_merge_kernel<<<n_tokens, kMergeThreads, smem, static_cast<cudaStream_t>(stream)>>>(
       shard_scores, shard_stride, row_stride, shard_topk, n_shards, n_tokens, top_k, shard_sel, merged);

@@ -526,8 +526,10 @@ smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_r
       return SMLA_ERR_CUDA;
   }
   const size_t smem = sizeof(IdxSmem) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
+  static std::atomic<bool> attr_set[kMaxDeviceSlots] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return SMLA_ERR_CUDA;
+  if (!attr_set[dev].load(std::memory_order_acquire)) {
     if (cudaFuncSetAttribute(index_scores_kernel<kH, kD, kBS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
@@ -536,7 +538,7 @@ smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_r
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, index_scores_kernel<kH, kD, kBS>) != cudaSuccess) return SMLA_ERR_CUDA;
     if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
-    attr_set = true;
+    attr_set[dev].store(true, std::memory_order_release);
   }
   index_scores_kernel<kH, kD, kBS><<<grid, kThreads, smem, stream>>>(A, key_map, q_map);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
@@ -545,13 +547,16 @@ smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_r
 }  // namespace
 
 EncodeTiledFn encode_tiled() {
-  static EncodeTiledFn fn = nullptr;
+  static std::atomic<EncodeTiledFn> cached{nullptr};  // the driver's entry point, one per process
+  EncodeTiledFn fn = cached.load(std::memory_order_acquire);
   if (fn == nullptr) {
     void* p = nullptr;
     cudaDriverEntryPointQueryResult q;
     if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
+        q == cudaDriverEntryPointSuccess) {
       fn = reinterpret_cast<EncodeTiledFn>(p);
+      cached.store(fn, std::memory_order_release);
+    }
   }
   return fn;
 }

@@ -1,6 +1,7 @@
 // Internal declarations shared by the libsmla translation units.
 #pragma once
 
+#include <atomic>
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
@@ -44,6 +45,11 @@ EncodeTiledFn encode_tiled();
 // Device error word (defined in api.cu); launchers receive its address.
 unsigned* device_error_word();
 int device_sm_count();
+// Launch attributes (shared-memory opt-in, occupancy) belong to a device: launchers keep
+// them per device, in tables of kMaxDeviceSlots entries indexed by current_device_index().
+constexpr int kMaxDeviceSlots = 64;
+// The calling thread's current device, or -1 if it cannot be read or is beyond the table.
+int current_device_index();
 
 smla_status_t launch_kvpack_store(const KernelLayout& L, void* pool, int layer, const void* latent,
                                   const void* rope, const uint8_t* idx_k, const float* idx_scale,

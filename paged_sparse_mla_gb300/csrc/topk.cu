@@ -535,11 +535,11 @@ __global__ void __launch_bounds__(kThreads, 2) topk_kernel(int k, const float* _
 }  // namespace
 
 int topk_wave() {
-  constexpr int kMaxDev = 64;
-  static int wave[kMaxDev] = {};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDev) return 0;
-  if (wave[dev] == 0) {
+  static std::atomic<int> wave[kMaxDeviceSlots] = {};
+  const int dev = current_device_index();
+  if (dev < 0) return 0;
+  int w = wave[dev].load(std::memory_order_acquire);
+  if (w == 0) {
     const size_t smem = sizeof(TopkSmem);
     if (cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem)) !=
             cudaSuccess ||
@@ -550,9 +550,10 @@ int topk_wave() {
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, topk_kernel<true>, kThreads, smem) != cudaSuccess ||
         per_sm <= 0)
       return 0;
-    wave[dev] = per_sm * device_sm_count();
+    w = per_sm * device_sm_count();
+    wave[dev].store(w, std::memory_order_release);
   }
-  return wave[dev];
+  return w;
 }
 
 smla_status_t launch_topk(int top_k, const float* scores, int64_t scores_stride, const int32_t* seq_lens,
