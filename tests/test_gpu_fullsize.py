@@ -4,7 +4,10 @@ The whole step runs on the GPU through smla_decode for every query token of
 the named workloads; the oracle recomputes chosen rows one by one (its pool
 holds the sampled sequence's cached context, written by the oracle's store).
 Indexer scores of those rows are compared bit for bit, top-k exactly,
-attention within the stated tolerance.
+attention within the stated tolerance.  Every other row's selection is checked
+against its own GPU score row with the exact top-k characterisation of
+tests/topk_properties.py (count, order, range, threshold, ties), which holds
+at any size.
 """
 import numpy as np
 import pytest
@@ -14,6 +17,7 @@ import oracle
 from paged_sparse_mla_gb300.workloads import make_config
 from tests.oracle_helpers import bits, layout_of, npy, oracle_pool, sequence_slots
 from tests import gpu_helpers as G
+from tests.topk_properties import assert_topk_exact
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -53,6 +57,9 @@ def test_full_size_sampled_rows(cfg):
     assert G.smla.smla_get_last_error() == 0
     rows = _sample_rows(wl, cfg)
     seqs, pos = oracle.query_positions(npy(wl.seq_lens), npy(wl.query_start_loc))
+    # every row: the fused step's selection is the top-k of its score row
+    assert_topk_exact(scores, torch.from_numpy(res["topk"]).cuda(), torch.from_numpy(pos + 1), wl.dims.top_k,
+                      f"config {cfg}")
     lo = layout_of(wl)
     by_seq = {}
     for t in rows:
