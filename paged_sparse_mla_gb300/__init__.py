@@ -1,7 +1,9 @@
 """Python binding of libsmla, the GB300 paged top-k sparse-MLA library.
 
-Argument marshalling only: every function takes torch CUDA tensors, checks
-dtypes and shapes, and calls the same-named C entry point of
+Argument marshalling only: every function takes torch CUDA tensors on the
+current device, checks their dtypes and that each holds at least the elements
+the kernels read or write through it (a short buffer raises here instead of
+being overrun on the GPU), and calls the same-named C entry point of
 ``include/smla.h`` through ctypes.  All computation happens in the library's
 CUDA kernels; there is no CPU path.  If ``_build/libsmla.so`` is missing the
 import of ``lib()`` raises -- build it with ``paged_sparse_mla_gb300.build_lib.build()``.
@@ -116,6 +118,8 @@ def _ptr(t):
         return None
     if not t.is_cuda:
         raise ValueError("libsmla takes CUDA tensors only")
+    if t.device.index != torch.cuda.current_device():
+        raise ValueError(f"tensor on {t.device}, but the current device is cuda:{torch.cuda.current_device()}")
     if not t.is_contiguous():
         raise ValueError("libsmla takes contiguous tensors only")
     return ctypes.c_void_p(t.data_ptr())
@@ -130,6 +134,49 @@ def _stream(stream):
 def _expect(t, dtype, name):
     if t.dtype != dtype:
         raise TypeError(f"{name}: expected {dtype}, got {t.dtype}")
+
+
+def _need(t, dtype, name, numel=0, dims=None):
+    """A tensor argument's dtype, rank and minimum element count (the kernels read or write that many
+    elements through its pointer).  None passes: the argument is optional or checked by the library."""
+    if t is None:
+        return
+    _expect(t, dtype, name)
+    if dims is not None and t.dim() != dims:
+        raise ValueError(f"{name}: expected {dims} dimensions, got shape {tuple(t.shape)}")
+    if t.numel() < numel:
+        raise ValueError(f"{name}: needs at least {numel} elements, got shape {tuple(t.shape)}")
+
+
+def _need_geometry(block_table, seq_lens, query_start_loc, batch):
+    """block_table [>= batch, bt_stride], seq_lens [>= batch] and query_start_loc [>= batch + 1], int32."""
+    _need(block_table, torch.int32, "block_table", dims=2)
+    if block_table.shape[0] < batch:
+        raise ValueError(f"block_table: needs a row per sequence ({batch}), got shape {tuple(block_table.shape)}")
+    _need(seq_lens, torch.int32, "seq_lens", batch)
+    _need(query_start_loc, torch.int32, "query_start_loc", batch + 1)
+
+
+def _need_step(layout, params, pool, q, q_pe, q_idx, w, out, lse, topk_idx_out):
+    """The per-query-token arrays of a fused step with T = q.shape[0] query tokens."""
+    T, H, HI = q.shape[0], params.n_heads, params.n_idx_heads
+    _need(pool, torch.uint8, "pool", layout.pool_bytes)
+    _need(q, torch.bfloat16, "q", T * H * layout.d_latent)
+    _need(q_pe, torch.bfloat16, "q_pe", T * H * layout.d_rope)
+    _need(q_idx, torch.uint8, "q_idx", T * HI * layout.d_index)
+    _need(w, torch.float32, "w", T * HI)
+    _need(out, torch.bfloat16, "out", T * H * layout.d_latent)
+    _need(lse, torch.float32, "lse", T * H)
+    _need(topk_idx_out, torch.int32, "topk_idx_out", T * params.top_k)
+
+
+def _need_new_tokens(layout, n, latent, rope, idx_k, idx_scale, slot_mapping, what="new"):
+    """The n new tokens a step stores: latent, rope, indexer key and scale, slot per token."""
+    _need(slot_mapping, torch.int64, "slot_mapping", n)
+    _need(latent, torch.bfloat16, f"{what}_latent", n * layout.d_latent)
+    _need(rope, torch.bfloat16, f"{what}_rope", n * layout.d_rope)
+    _need(idx_k, torch.uint8, f"{what}_idx_k", n * layout.d_index)
+    _need(idx_scale, torch.float32, f"{what}_idx_scale", n)
 
 
 def version() -> int:
@@ -156,24 +203,27 @@ def workspace_size(layout: Layout, params: Params, n_tokens: int, max_ctx: int) 
 
 
 def kvpack_store(layout, pool, layer, latent, rope, idx_k, idx_scale, slot_mapping, stream=None):
-    _expect(pool, torch.uint8, "pool")
-    _expect(latent, torch.bfloat16, "latent")
-    _expect(rope, torch.bfloat16, "rope")
-    _expect(idx_k, torch.uint8, "idx_k")
-    _expect(idx_scale, torch.float32, "idx_scale")
     _expect(slot_mapping, torch.int64, "slot_mapping")
     n = slot_mapping.numel()
+    _need(pool, torch.uint8, "pool", layout.pool_bytes)
+    _need(latent, torch.bfloat16, "latent", n * layout.d_latent)
+    _need(rope, torch.bfloat16, "rope", n * layout.d_rope)
+    _need(idx_k, torch.uint8, "idx_k", n * layout.d_index)
+    _need(idx_scale, torch.float32, "idx_scale", n)
     _check(lib().kvpack_store(ctypes.byref(layout), _ptr(pool), layer, _ptr(latent), _ptr(rope), _ptr(idx_k),
                               _ptr(idx_scale), _ptr(slot_mapping), n, _stream(stream)), "kvpack_store")
 
 
 def smla_index_scores(layout, params, pool, layer, q_idx, w, block_table, seq_lens, query_start_loc, max_q,
                       max_ctx, scores, stream=None):
-    _expect(q_idx, torch.uint8, "q_idx")
-    _expect(w, torch.float32, "w")
-    _expect(block_table, torch.int32, "block_table")
-    _expect(scores, torch.float32, "scores")
     n_tokens = q_idx.shape[0]
+    _need(pool, torch.uint8, "pool", layout.pool_bytes)
+    _need(q_idx, torch.uint8, "q_idx", n_tokens * params.n_idx_heads * layout.d_index)
+    _need(w, torch.float32, "w", n_tokens * params.n_idx_heads)
+    _need_geometry(block_table, seq_lens, query_start_loc, seq_lens.numel())
+    _need(scores, torch.float32, "scores", dims=2)
+    if scores.shape[0] < n_tokens:
+        raise ValueError(f"scores: needs a row per query token ({n_tokens}), got shape {tuple(scores.shape)}")
     _check(lib().smla_index_scores(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(q_idx),
                                    _ptr(w), _ptr(block_table), block_table.shape[1], _ptr(seq_lens),
                                    _ptr(query_start_loc), seq_lens.numel(), n_tokens, max_q, max_ctx, _ptr(scores),
@@ -187,8 +237,16 @@ def topk_workspace_size(params, n_tokens) -> int:
 def smla_topk(params, scores, seq_lens, query_start_loc, topk_idx, stream=None, workspace=None):
     """Exact top-k per row.  `workspace` (uint8 device tensor of at least topk_workspace_size(...)
     bytes, optional) lets a small batch of long rows split each row over CTAs."""
-    _expect(scores, torch.float32, "scores")
-    _expect(topk_idx, torch.int32, "topk_idx")
+    _need(topk_idx, torch.int32, "topk_idx", dims=2)
+    rows = topk_idx.shape[0]
+    if topk_idx.shape[1] != params.top_k:
+        raise ValueError(f"topk_idx: rows of top_k = {params.top_k} entries expected, got shape {tuple(topk_idx.shape)}")
+    _need(scores, torch.float32, "scores", dims=2)
+    if scores.shape[0] < rows:
+        raise ValueError(f"scores: needs a row per top-k row ({rows}), got shape {tuple(scores.shape)}")
+    _need(seq_lens, torch.int32, "seq_lens")
+    _need(query_start_loc, torch.int32, "query_start_loc", seq_lens.numel() + 1)
+    _need(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().smla_topk(ctypes.byref(params), _ptr(scores), scores.stride(0), _ptr(seq_lens),
                            _ptr(query_start_loc), seq_lens.numel(), topk_idx.shape[0], _ptr(topk_idx),
@@ -199,14 +257,28 @@ def attend_workspace_size(layout, params, n_tokens) -> int:
     return int(lib().smla_attend_workspace_size(ctypes.byref(layout), ctypes.byref(params), n_tokens))
 
 
+def _need_attend(layout, params, pool, q, q_pe, topk_idx, block_table, query_start_loc, out, lse):
+    """Arrays of smla_attend with T = q.shape[0] query tokens and B = query_start_loc.numel() - 1 sequences."""
+    T, H = q.shape[0], params.n_heads
+    _need(pool, torch.uint8, "pool", layout.pool_bytes)
+    _need(q, torch.bfloat16, "q", T * H * layout.d_latent)
+    _need(q_pe, torch.bfloat16, "q_pe", T * H * layout.d_rope)
+    _need(topk_idx, torch.int32, "topk_idx", T * params.top_k)
+    _need(query_start_loc, torch.int32, "query_start_loc", 1)
+    batch = query_start_loc.numel() - 1
+    _need(block_table, torch.int32, "block_table", dims=2)
+    if block_table.shape[0] < batch:
+        raise ValueError(f"block_table: needs a row per sequence ({batch}), got shape {tuple(block_table.shape)}")
+    _need(out, torch.bfloat16, "out", T * H * layout.d_latent)
+    _need(lse, torch.float32, "lse", T * H)
+
+
 def smla_attend(layout, params, pool, layer, q, q_pe, topk_idx, block_table, query_start_loc, out, lse,
                 stream=None, workspace=None):
     """Latent attention over the selected positions.  `workspace` (uint8 device tensor of at least
     attend_workspace_size(...) bytes, optional) lets a small batch split each token over CTAs."""
-    _expect(q, torch.bfloat16, "q")
-    _expect(q_pe, torch.bfloat16, "q_pe")
-    _expect(out, torch.bfloat16, "out")
-    _expect(lse, torch.float32, "lse")
+    _need_attend(layout, params, pool, q, q_pe, topk_idx, block_table, query_start_loc, out, lse)
+    _need(workspace, torch.uint8, "workspace")
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     _check(lib().smla_attend(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(q), _ptr(q_pe),
                              _ptr(topk_idx), _ptr(block_table), block_table.shape[1], _ptr(query_start_loc),
@@ -218,8 +290,8 @@ def smla_attend(layout, params, pool, layer, q, q_pe, topk_idx, block_table, que
 def smla_attend_hisparse(layout, params, pool, layer, host_records, host_block_map, q, q_pe, topk_idx, block_table,
                          query_start_loc, out, lse, stream=None):
     """smla_attend with the records of mapped blocks read from a pinned host buffer (host_records, uint8)."""
-    _expect(q, torch.bfloat16, "q")
-    _expect(host_block_map, torch.int32, "host_block_map")
+    _need_attend(layout, params, pool, q, q_pe, topk_idx, block_table, query_start_loc, out, lse)
+    _need(host_block_map, torch.int32, "host_block_map", layout.num_blocks)
     _expect(host_records, torch.uint8, "host_records")
     if host_records.is_cuda or not host_records.is_pinned():
         raise ValueError("host_records must be pinned host memory")
@@ -237,8 +309,12 @@ def smla_attend_hisparse(layout, params, pool, layer, host_records, host_block_m
 def smla_decode(layout, params, pool, layer, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping, q, q_pe,
                 q_idx, w, block_table, seq_lens, query_start_loc, max_q, max_ctx, out, lse, workspace,
                 topk_idx_out=None, stream=None):
-    _expect(q, torch.bfloat16, "q")
-    _expect(workspace, torch.uint8, "workspace")
+    T = q.shape[0]
+    _need_step(layout, params, pool, q, q_pe, q_idx, w, out, lse, topk_idx_out)
+    _need_geometry(block_table, seq_lens, query_start_loc, seq_lens.numel())
+    if slot_mapping is not None:
+        _need_new_tokens(layout, T, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping)
+    _need(workspace, torch.uint8, "workspace")
     _check(lib().smla_decode(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(new_latent),
                              _ptr(new_rope), _ptr(new_idx_k), _ptr(new_idx_scale), _ptr(slot_mapping), _ptr(q),
                              _ptr(q_pe), _ptr(q_idx), _ptr(w), _ptr(block_table), block_table.shape[1],
@@ -255,7 +331,11 @@ def smla_decode_static(layout, params, pool, layer, new_latent, new_rope, new_id
     The scores and top-k scratch live in the library's static 64 MiB device
     array; calls share it, so calls that overlap on the GPU race on it.
     """
-    _expect(q, torch.bfloat16, "q")
+    T = q.shape[0]
+    _need_step(layout, params, pool, q, q_pe, q_idx, w, out, lse, topk_idx_out)
+    _need_geometry(block_table, seq_lens, query_start_loc, seq_lens.numel())
+    if slot_mapping is not None:
+        _need_new_tokens(layout, T, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping)
     _check(lib().smla_decode_static(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(new_latent),
                                     _ptr(new_rope), _ptr(new_idx_k), _ptr(new_idx_scale), _ptr(slot_mapping), _ptr(q),
                                     _ptr(q_pe), _ptr(q_idx), _ptr(w), _ptr(block_table), block_table.shape[1],
@@ -268,9 +348,11 @@ def smla_prefill_chunk(layout, params, pool, layer, chunk_latent, chunk_rope, ch
                        slot_mapping, q, q_pe, q_idx, w, block_table, seq_lens, query_start_loc, chunk_len, max_ctx,
                        out, lse, workspace, topk_idx_out=None, stream=None):
     """A prefill chunk per sequence (its keys stored first), causal within the chunk."""
-    _expect(q, torch.bfloat16, "q")
-    _expect(workspace, torch.uint8, "workspace")
-    _expect(slot_mapping, torch.int64, "slot_mapping")
+    T = q.shape[0]
+    _need_step(layout, params, pool, q, q_pe, q_idx, w, out, lse, topk_idx_out)
+    _need_geometry(block_table, seq_lens, query_start_loc, seq_lens.numel())
+    _need_new_tokens(layout, T, chunk_latent, chunk_rope, chunk_idx_k, chunk_idx_scale, slot_mapping, "chunk")
+    _need(workspace, torch.uint8, "workspace")
     _check(lib().smla_prefill_chunk(ctypes.byref(layout), ctypes.byref(params), _ptr(pool), layer, _ptr(chunk_latent),
                                     _ptr(chunk_rope), _ptr(chunk_idx_k), _ptr(chunk_idx_scale), _ptr(slot_mapping),
                                     _ptr(q), _ptr(q_pe), _ptr(q_idx), _ptr(w), _ptr(block_table), block_table.shape[1],
@@ -281,10 +363,14 @@ def smla_prefill_chunk(layout, params, pool, layer, chunk_latent, chunk_rope, ch
 
 def smla_dcp_topk_merge(shard_scores, shard_topk, shard_sel, merged=None, stream=None):
     """Candidate merge over token shards.  shard_scores [N, T, stride] fp32, shard_topk / shard_sel [N, T, k] int32."""
-    _expect(shard_scores, torch.float32, "shard_scores")
-    _expect(shard_topk, torch.int32, "shard_topk")
-    _expect(shard_sel, torch.int32, "shard_sel")
+    _need(shard_topk, torch.int32, "shard_topk", dims=3)
     n, t, k = shard_topk.shape
+    _need(shard_scores, torch.float32, "shard_scores", dims=3)
+    if shard_scores.shape[0] < n or shard_scores.shape[1] < t:
+        raise ValueError(f"shard_scores: needs [{n}, {t}, >= visible] for shard_topk {tuple(shard_topk.shape)}, "
+                         f"got {tuple(shard_scores.shape)}")
+    _need(shard_sel, torch.int32, "shard_sel", n * t * k)
+    _need(merged, torch.int32, "merged", t * k)
     _check(lib().smla_dcp_topk_merge(_ptr(shard_scores), shard_scores.stride(0), shard_scores.stride(1),
                                      _ptr(shard_topk), n, t, k, _ptr(shard_sel), _ptr(merged), _stream(stream)),
            "smla_dcp_topk_merge")
@@ -292,11 +378,11 @@ def smla_dcp_topk_merge(shard_scores, shard_topk, shard_sel, merged=None, stream
 
 def smla_lse_merge(parts_out, parts_lse, out, lse, stream=None):
     """LSE merge of partial outputs.  parts_out [N, T, H, D] bf16, parts_lse [N, T, H] fp32."""
-    _expect(parts_out, torch.bfloat16, "parts_out")
-    _expect(parts_lse, torch.float32, "parts_lse")
-    _expect(out, torch.bfloat16, "out")
-    _expect(lse, torch.float32, "lse")
+    _need(parts_out, torch.bfloat16, "parts_out", dims=4)
     n, t, h, d = parts_out.shape
+    _need(parts_lse, torch.float32, "parts_lse", n * t * h)
+    _need(out, torch.bfloat16, "out", t * h * d)
+    _need(lse, torch.float32, "lse", t * h)
     _check(lib().smla_lse_merge(_ptr(parts_out), _ptr(parts_lse), n, t, h, d, _ptr(out), _ptr(lse), _stream(stream)),
            "smla_lse_merge")
 
