@@ -46,6 +46,13 @@
  * sequence b sits at position p = seq_lens[b] - n_q + i and sees positions
  * 0..p (itself included).  block_table[b * bt_stride + j / block_size] is the
  * physical block of logical position j.
+ *
+ * Values that are trusted, not checked: query_start_loc increases from 0 to
+ * n_tokens, every sequence has at least as many cached tokens as query tokens,
+ * and max_ctx (where a call takes it) is at least every seq_lens entry.  The
+ * kernels size their loops from these values, so a call that breaks them
+ * reads and writes outside the score rows and block-table rows it was given.
+ * Block ids and slots, by contrast, are checked on the device (see above).
  */
 #ifndef SMLA_H
 #define SMLA_H
