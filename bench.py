@@ -443,14 +443,18 @@ def run_gpu(args):
 
 # ----------------------------------------------------------------------------- oracle (CPU) arm
 class OracleSampler:
-    """The CPU oracle on whole sequences of a workload.
+    """The CPU oracle on the query tokens of a workload.
 
     The workload is generated once, and each sampled sequence's cached context is written into its
     own oracle pool once, on first use (set-up, outside the timed region).  `run` then times the
-    oracle's full step (store of the sequence's new tokens, indexer, top-k, attention for each of
-    its query tokens) over sequences taken in a fixed random order, cycling over the first
-    `max_seqs` of them, until `budget_s` seconds of oracle work are done.
+    oracle's step over sequences taken in a fixed random order, cycling over the first `max_seqs`
+    of them, until `budget_s` seconds of oracle work are done.  A sequence's query tokens go in
+    slices of at most `max_rows` (all of a decode step's tokens; consecutive rows of a prefill
+    chunk): the first slice of a pass over the sequence also stores its new tokens, and every slice
+    runs the indexer, top-k and attention of its rows.
     """
+
+    max_rows = 4
 
     def __init__(self, workload: int, max_seqs: int):
         from paged_sparse_mla_gb300.workloads import make_config
@@ -463,6 +467,7 @@ class OracleSampler:
         self.order = [int(b) for b in np.random.default_rng(7).permutation(wl.batch)[:max_seqs]]
         self.qsl = self._npy(wl.query_start_loc)
         self.next = 0
+        self.row_cursor = {}
         self.pools = {}
         self.args = dict(latent_new=self._bits(wl.new_latent), rope_new=self._bits(wl.new_rope),
                          idxk_new=self._npy(wl.new_idx_k), idxs_new=self._npy(wl.new_idx_s), q=self._bits(wl.q),
@@ -501,14 +506,21 @@ class OracleSampler:
         done_tokens, spent, seqs = 0, 0.0, []
         while spent < budget_s:
             b = self.order[self.next % len(self.order)]
-            self.next += 1
             pool, sm = self._pool(b)
-            rows = list(range(int(self.qsl[b]), int(self.qsl[b + 1])))
+            q0, q1 = int(self.qsl[b]), int(self.qsl[b + 1])
+            r0 = self.row_cursor.get(b, 0)
+            rows = list(range(q0 + r0, min(q1, q0 + r0 + self.max_rows)))
+            store = sm if r0 == 0 else np.full_like(sm, -1)
             t0 = time.perf_counter()
-            self.oracle.decode_step(self.lay, pool, 0, slot_mapping=sm, rows=rows, **self.args)
+            self.oracle.decode_step(self.lay, pool, 0, slot_mapping=store, rows=rows, **self.args)
             spent += time.perf_counter() - t0
             done_tokens += len(rows)
-            seqs.append(b)
+            if r0 + len(rows) >= q1 - q0:           # the sequence is done: the next one, from its start
+                self.row_cursor[b] = 0
+                self.next += 1
+                seqs.append(b)
+            else:
+                self.row_cursor[b] = r0 + len(rows)
         return done_tokens, spent, seqs
 
 
@@ -517,8 +529,9 @@ def cpu_baseline(workload: int, budget_s: float):
     n, spent, seqs = sampler.run(budget_s)
     cores = len(os.sched_getaffinity(0))
     return {"value": round(n / spent, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{len(seqs)} whole sequences ({n} query tokens) of {sampler.wl.name}, full store+indexer+top-k+"
-                      f"attention per query token in numpy float64 ({spent:.1f} s); numpy BLAS may use all {cores} cores"}
+            "sample": f"{n} query tokens of {sampler.wl.name} ({len(seqs)} sequences completed; query tokens in slices "
+                      f"of at most {sampler.max_rows}), full store+indexer+top-k+attention per query token in numpy "
+                      f"float64 ({spent:.1f} s); numpy BLAS may use all {cores} cores"}
 
 
 def run_reference(args):
@@ -544,8 +557,8 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": name, "sample_per_step_s": round(per_step, 2)},
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
-                         "sample": f"per step: whole sequences of {name} (cycling over {len(sampler.order)} "
-                                   f"sequences, {len(set(seqs_all))} of them timed) until {per_step:.1f} s of "
+                         "sample": f"per step: query tokens of {name} in slices of at most {sampler.max_rows} "
+                                   f"(cycling over {len(sampler.order)} sequences) until {per_step:.1f} s of "
                                    f"oracle work; {tok} query tokens in {spent_total:.1f} s"},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
