@@ -17,11 +17,13 @@ that time.
 
 import argparse
 import hashlib
+import datetime
 import json
 import math
 import os
 import statistics
 import subprocess
+import tempfile
 import sys
 import time
 
@@ -71,22 +73,67 @@ def peaks():
 
 
 # ----------------------------------------------------------------------------- clocks
-class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+CLOCK_FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+CLOCK_REASONS = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
 
-    def __init__(self, device_index: int):
-        self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+def summarise_clocks(lines, t0=None, t1=None):
+    """Median SM clock, maximum SM clock and active throttle reasons of nvidia-smi samples.
+
+    `lines` are rows of CLOCK_FIELDS (csv, noheader, nounits).  With a window [t0, t1] of host
+    times (seconds since the epoch) only the samples taken inside it count; if none of them falls
+    inside (or their timestamps cannot be read) every sample counts, and `in_window` says so.
+    """
+    rows = []
+    for line in lines:
+        parts = [x.strip() for x in line.split(",")]
+        if len(parts) < 10:
+            continue
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            sm, mx = float(parts[2]), float(parts[3])
+        except ValueError:
+            continue
+        try:
+            ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+        except ValueError:
+            ts = None
+        active = {nm for nm, val in zip(CLOCK_REASONS, parts[6:10]) if val.lower().startswith("active")}
+        rows.append((ts, sm, mx, active))
+    if not rows:
+        return None
+    inside = rows
+    if t0 is not None and t1 is not None:
+        inside = [r for r in rows if r[0] is not None and t0 <= r[0] <= t1]
+    in_window = bool(inside) and t0 is not None
+    use = inside if inside else rows
+    reasons = set().union(*(r[3] for r in use))
+    return {"sm_mhz": statistics.median(r[1] for r in use), "sm_max_mhz": max(r[2] for r in use),
+            "reasons": sorted(reasons), "samples": len(use), "in_window": in_window}
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 50 ms, summarised over a marked window."""
+
+    def __init__(self, device_index: int, csv_path=None):
+        self.proc = None
+        self.t0 = self.t1 = None
+        self.path = csv_path or os.path.join(tempfile.gettempdir(), f"smla_clocks_{os.getpid()}.csv")
+        try:
+            os.makedirs(os.path.dirname(os.path.abspath(self.path)), exist_ok=True)
             self.fh = open(self.path, "w")
-            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"], stdout=self.fh,
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(device_index), f"--query-gpu={CLOCK_FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.fh,
                                          stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def start_window(self):
+        self.t0 = time.time()
+
+    def end_window(self):
+        self.t1 = time.time()
 
     def stop(self):
         if self.proc is None:
@@ -97,24 +144,8 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
-            except ValueError:
-                continue
-            for nm, val in zip(names, parts[5:9]):
-                if val.lower().startswith("active"):
-                    reasons.add(nm)
-        if not sm:
-            return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        with open(self.path) as f:
+            return summarise_clocks(f.readlines(), self.t0, self.t1)
 
 
 # ----------------------------------------------------------------------------- accounting
@@ -254,7 +285,7 @@ def run_gpu(args):
         raise RuntimeError(f"device error during warm-up: {smla.status_string(err)}")
 
     # ---------------- timed region: K fused steps ----------------
-    clocks = ClockSampler(local_rank) if rank == 0 else None
+    clocks = ClockSampler(local_rank, args.clocks_csv) if rank == 0 else None
     time.sleep(0.3)
     if world > 1:
         dist.barrier()
@@ -262,11 +293,15 @@ def run_gpu(args):
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
     torch.cuda._sleep(4_000_000)   # the host enqueues ahead of the GPU from the first step on
+    if clocks:
+        clocks.start_window()
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize()
+    if clocks:
+        clocks.end_window()
     if world > 1:
         dist.barrier()
     clk = clocks.stop() if clocks else None
@@ -636,16 +671,18 @@ def run_dcp(args):
     torch.cuda.synchronize()
     if smla.smla_get_last_error() != 0:
         raise RuntimeError("device error during warm-up")
-    clocks = ClockSampler(0)
+    clocks = ClockSampler(0, args.clocks_csv)
     time.sleep(0.3)
     torch.cuda._sleep(4_000_000)
     marks = [[ev() for _ in range(len(phases) + 1)] for _ in range(args.steps)]
+    clocks.start_window()
     for st in range(args.steps):
         marks[st][0].record(stream)
         for i, (_, f) in enumerate(phases):
             f()
             marks[st][i + 1].record(stream)
     torch.cuda.synchronize()
+    clocks.end_window()
     clk = clocks.stop()
     if smla.smla_get_last_error() != 0:
         raise RuntimeError("device error in the timed region")
@@ -745,10 +782,12 @@ def run_hisparse(args):
     rng = np.random.default_rng(29)
     moved = used[rng.random(used.size) < args.host_frac]
     host, hmap = evict_records(lay, pool, moved)
-    clocks = ClockSampler(0)
+    clocks = ClockSampler(0, args.clocks_csv)
     time.sleep(0.3)
+    clocks.start_window()
     ms_tier = timed(lambda: smla.smla_attend_hisparse(lay, prm, pool, 0, host, hmap, wl.q, wl.q_pe, topk,
                                                       wl.block_table, wl.query_start_loc, out, lse, stream=stream))
+    clocks.end_window()
     clk = clocks.stop()
     if smla.smla_get_last_error() != 0:
         raise RuntimeError("device error in the timed region")
@@ -777,11 +816,13 @@ def run_hisparse(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--workload", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--impl", default="smla", choices=["smla", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--clocks-csv", default=None,
+                    help="where to keep the raw nvidia-smi clock samples (default: a file in the temp directory)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--host-frac", type=float, default=0.0,
                     help="host-tier arm: fraction of the blocks whose records live in pinned host memory")
