@@ -91,6 +91,24 @@ def test_store_then_read_returns_quantised_inputs():
     assert np.array_equal(ks, wl.slot_idx_s[st].double().numpy())
 
 
+def test_full_record_round_trip_within_the_e4m3_bound():
+    """Four per-128 scale tiles: every element comes back within the E4M3 rounding bound of its
+    bf16 input, scaled by its own tile's scale (a read with another tile's scale breaks the bound)."""
+    from paged_sparse_mla_gb300.workloads import build_workload
+    wl = build_workload("round-trip", FULL, [300, 200], [1, 1], seed=11)
+    lay = layout_of(wl)
+    pool = oracle_pool(wl)
+    s = npy(wl.cached_slots)
+    st = torch.as_tensor(s)
+    lat, rope = oracle.read_record(lay, pool, 0, s)
+    x = bf16_bits_to_f64(bits(wl.slot_latent[st])).reshape(len(s), 4, 128)
+    amax = np.abs(x).max(axis=2, keepdims=True)
+    scale = amax / 448.0
+    bound = np.maximum(np.abs(x) * 2.0 ** -4, scale * 2.0 ** -10) * (1 + 1e-6)
+    assert (np.abs(lat.reshape(len(s), 4, 128) - x) <= bound).all()
+    assert np.array_equal(rope, bf16_bits_to_f64(bits(wl.slot_rope[st])))
+
+
 def test_store_skips_negative_slots_and_touches_only_its_bytes():
     wl = make_config(1)
     lay = layout_of(wl)

@@ -109,6 +109,20 @@ def test_pin_catches_planted_mistake(monkeypatch, name, mod, attr, bad, pin):
         pin()
 
 
+def test_pin_catches_dequant_with_the_first_tile_scale(monkeypatch):
+    def bad_read(layout, pool, layer, slots):
+        lat, rope = orig(layout, pool, layer, slots)
+        rec = oracle.store._offsets(layout, slots, layer, "record")[:, None]
+        codes = pool[rec + np.arange(layout.d_latent)]
+        s0 = np.ascontiguousarray(pool[rec + layout.d_latent + np.arange(4)]).view(np.float32)
+        return (oracle.e4m3_decode(codes) * s0.astype(np.float64)).astype(np.float32).astype(np.float64), rope
+    orig = oracle.store.read_record
+    monkeypatch.setattr(oracle.store, "read_record", bad_read)
+    monkeypatch.setattr(oracle, "read_record", bad_read)
+    with pytest.raises(AssertionError):
+        ts.test_full_record_round_trip_within_the_e4m3_bound()
+
+
 def test_pin_catches_wrong_scale_rounding(monkeypatch):
     def bad_quant(latent_bits, quant_tile):
         codes, scale = orig(latent_bits, quant_tile)

@@ -76,3 +76,9 @@ def test_block_ids_are_a_permutation_and_new_slots_are_free():
     assert used.size == wl.num_blocks                      # every pool block belongs to some sequence
     assert not np.isin(wl.slot_mapping.numpy(), wl.cached_slots.numpy()).any()
     assert np.array_equal(np.sort(wl.slot_mapping.numpy()), np.unique(wl.slot_mapping.numpy()))
+
+
+def test_softmax_scales():
+    # the tiny workload's text fixes 1/sqrt(80); the DeepSeek shape takes 1/sqrt(D_L + D_R) = 1/sqrt(576)
+    assert TINY.softmax_scale == pytest.approx(80 ** -0.5, rel=1e-15)
+    assert FULL.softmax_scale == pytest.approx(576 ** -0.5, rel=1e-15)
