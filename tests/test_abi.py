@@ -81,3 +81,23 @@ def test_host_side_argument_checks(lib):
     assert lib.smla_selftest_wait(20_000_000_000, None) == 1     # above 10 s
     assert lib.smla_status_string(4) == b"SMLA_ERR_BAD_INDEX"
     assert lib.smla_version() >= 100
+
+
+def test_header_is_c99_and_the_library_links_from_c(lib, tmp_path):
+    """A plain C caller (tests/c/abi_host_check.c) compiles against include/smla.h with gcc -std=c99
+    -pedantic -Werror, links libsmla.so and gets the documented host-side answers."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    src = os.path.join(build_lib.ROOT, "tests", "c", "abi_host_check.c")
+    exe = str(tmp_path / "abi_host_check")
+    lib_dir = os.path.dirname(build_lib.LIB)
+    cc = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-pedantic", "-I",
+                         os.path.dirname(HEADER), src, "-L", lib_dir, "-lsmla", f"-Wl,-rpath,{lib_dir}", "-o", exe],
+                        capture_output=True, text=True)
+    assert cc.returncode == 0, cc.stderr
+    run = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert run.returncode == 0, run.stderr
+    assert "abi host check ok" in run.stdout
