@@ -254,8 +254,9 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
 
 /*
  * smla_prefill_chunk -- chunked prefill on a cached prefix, one layer
- * ([GLM-5.3 "Config and numbers"] and [AgentX "Serving numbers"]: 8K-token
- * prefill chunks over long cached prefixes).  Each sequence b appends a chunk
+ * ([AgentX "Head-of-line blocking"]: the chunked-prefill scheduler splits long
+ * prefills into per-step token budgets; [GLM-5.3 "What is new"]: prefill of
+ * long prompts split into chunks).  Each sequence b appends a chunk
  * of n_b = query_start_loc[b+1] - query_start_loc[b] tokens whose KV is stored
  * first (chunk_latent/chunk_rope/chunk_idx_k/chunk_idx_scale at slot_mapping,
  * required); seq_lens[b] includes the chunk, and chunk token i attends the
