@@ -148,6 +148,43 @@ class ClockSampler:
             return summarise_clocks(f.readlines(), self.t0, self.t1)
 
 
+# ----------------------------------------------------------------------------- launch count
+LIB_KERNELS = ("kvpack_store_kernel", "index_scores_kernel", "topk_kernel", "attend_kernel", "split_merge_kernel",
+               "topk_merge_kernel", "lse_merge_kernel")
+
+
+def count_lib_kernels(names):
+    """How many of the given kernel names are this library's kernels."""
+    return sum(1 for n in names if any(k in n for k in LIB_KERNELS))
+
+
+def count_step_launches(step_fn) -> int:
+    """Kernels of this library that one call of step_fn launches (0 if the profiler saw none, or a
+    CUDA tool such as ncu is attached to the process: the two would both subscribe to CUPTI)."""
+    if os.environ.get("CUDA_INJECTION64_PATH"):
+        return 0
+    try:
+        from torch.profiler import ProfilerActivity, profile
+        torch.cuda.synchronize()
+        with profile(activities=[ProfilerActivity.CUDA]) as prof:
+            step_fn()
+            torch.cuda.synchronize()
+        return count_lib_kernels(e.name for e in prof.events() if e.device_type == torch.autograd.DeviceType.CUDA)
+    except Exception:                       # profiler unavailable: the caller falls back to the formula
+        return 0
+
+
+def plausible_launches(profiled: int, n_groups: int):
+    """(launches per fused step, how it was obtained).  The step launches the store once and, per query
+    group, the indexer, the top-k and the attention, plus at most a second top-k pass and an attention
+    merge; a profiled count outside that range is not taken."""
+    base = 1 + 3 * n_groups
+    if base <= profiled <= base + 2 * n_groups:
+        return profiled, "profiled one step"
+    note = f"; profiler count {profiled} outside [{base}, {base + 2 * n_groups}]" if profiled else ""
+    return base, "formula: store + 3 launches per query group" + note
+
+
 # ----------------------------------------------------------------------------- accounting
 def accounting(wl, topk_host):
     """Algorithmic bytes / flops per step for each kernel (see the design notes)."""
@@ -275,7 +312,6 @@ def run_gpu(args):
     stride = (wl.max_ctx + 3) // 4 * 4
     per_group = max(1, min(T, (512 << 20) // (stride * 4)))
     n_groups = math.ceil(T / per_group)
-    launches_per_step = 1 + 3 * n_groups
 
     for _ in range(args.warmup):
         step()
@@ -406,6 +442,10 @@ def run_gpu(args):
         dist.destroy_process_group()
         return
 
+    # launches of one fused step, counted by the profiler after all timing is done (the split paths
+    # for small batches add a merge launch to the attention and a second pass to the top-k)
+    launches_per_step, launches_how = plausible_launches(count_step_launches(step), n_groups)
+
     # ---------------- roofline of the dominant kernel ----------------
     acct = accounting(wl, topk.cpu().numpy())
     pk = peaks()
@@ -467,6 +507,7 @@ def run_gpu(args):
         "clocks": clk,
         "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": launches_per_step * args.steps,
+        "gpu_launches_how": f"{launches_per_step} per step ({launches_how}) x {args.steps} steps",
         "kernels": kernels,
         "roofline": roof,
         "cpu_baseline": cpu,

@@ -47,3 +47,22 @@ def test_unreadable_timestamps_and_short_rows():
     s = bench.summarise_clocks(lines, _t(0.0), _t(1.0))
     assert s["samples"] == 1 and not s["in_window"] and s["sm_mhz"] == 1800.0
     assert bench.summarise_clocks(["garbage"]) is None
+
+
+def test_launch_count_names_and_fallback():
+    names = ["void (anonymous namespace)::index_scores_kernel<64, 128, 64>(IdxArgs, CUtensorMap_st)",
+             "void (anonymous namespace)::topk_kernel<true>(int, float const*)", "Memset (Device)",
+             "void (anonymous namespace)::attend_kernel<9, true, false>(AttnArgs)",
+             "void smla::kvpack_store_kernel<16>(KernelLayout)", "void at::native::vectorized_elementwise_kernel"]
+    assert bench.count_lib_kernels(names) == 4
+    # no CUDA here: the profiler count gives 0 and the bench falls back to its formula
+    assert bench.count_step_launches(lambda: None) == 0
+
+
+def test_launch_count_must_fit_the_schedule():
+    assert bench.plausible_launches(4, 1) == (4, "profiled one step")
+    assert bench.plausible_launches(6, 1)[0] == 6                 # split top-k and split attention
+    assert bench.plausible_launches(0, 1)[0] == 4                 # no profiler: the formula
+    n, how = bench.plausible_launches(8, 1)                       # e.g. counted twice: not taken
+    assert n == 4 and "outside" in how
+    assert bench.plausible_launches(10, 3)[0] == 10
