@@ -244,7 +244,7 @@ def accounting(wl, topk_host):
 
 def traffic_table():
     """ncu DRAM bytes per launch recorded under profiles/, keyed by kernel source hash."""
-    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    path = os.path.join(ROOT, "profiles", "dram_bytes_per-launch_all-kernels_agentic-mtp4-b64-ctx142k.txt")
     out = {}
     if not os.path.exists(path):
         return out
