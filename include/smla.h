@@ -85,7 +85,10 @@ typedef enum smla_status {
  *
  * every region on a 256-byte boundary; a record is
  *   [d_latent e4m3 codes][d_latent/quant_tile fp32 scales][d_rope bf16] (padded to 16 B).
- * Filled in by smla_layout_init(); read-only afterwards.
+ * Filled in by smla_layout_init(); read-only afterwards.  Every entry point
+ * accepts a layout only as smla_layout_init filled it in: it recomputes the
+ * derived fields from the shape fields and refuses any difference with
+ * SMLA_ERR_INVALID_ARG.
  */
 typedef struct smla_layout {
   int32_t block_size;     /* tokens per block                                  */
@@ -188,7 +191,10 @@ size_t smla_topk_workspace_size(const smla_params_t* params, int n_tokens);
  * with K[j] the dequantised latent and kpe[j] the cached rope.
  *   q        bf16 [n_tokens, n_heads, d_latent]
  *   q_pe     bf16 [n_tokens, n_heads, d_rope]
- *   topk_idx int32 [n_tokens, top_k]; entries < 0 are ignored
+ *   topk_idx int32 [n_tokens, top_k]; entries < 0 are ignored.  An entry at or
+ *            beyond bt_stride * block_size (past the sequence's block-table
+ *            row) is not looked up: it latches SMLA_ERR_BAD_INDEX and its
+ *            record reads as zeros, like an out-of-range block id.
  *   out      bf16 [n_tokens, n_heads, d_latent]
  *   lse      fp32 [n_tokens, n_heads]  (natural log; -inf and out = 0 when no entry is valid)
  *   workspace, workspace_bytes: optional device scratch (NULL and 0 allowed).  With fewer
@@ -241,6 +247,11 @@ smla_status_t smla_attend_hisparse(const smla_layout_t* layout, const smla_param
  *   workspace: device scratch of at least smla_workspace_size(...) bytes,
  *     256-byte aligned
  * Query tokens are processed in groups so the score scratch stays bounded.
+ * Refused before anything is enqueued: a layout not made by smla_layout_init,
+ * n_heads, n_idx_heads or top_k <= 0, a NULL q_pe while d_rope > 0 (or a NULL
+ * new-token input while slot_mapping is given), bt_stride * block_size below
+ * max_ctx (SMLA_ERR_INVALID_ARG); head counts and dimensions the kernels are
+ * not built for (SMLA_ERR_UNSUPPORTED).
  */
 smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* params, void* pool,
                           int layer, const void* new_latent, const void* new_rope,
@@ -284,7 +295,9 @@ smla_status_t smla_prefill_chunk(const smla_layout_t* layout, const smla_params_
  * The pages have no counterpart of this entry point; it only changes where the
  * scratch lives.
  *   Arguments and results are those of smla_decode without workspace /
- *   workspace_bytes: the fp32 scores and top-k indices live in a 64 MiB static
+ *   workspace_bytes, checked in the same order and refused with the same
+ *   status (including SMLA_ERR_UNSUPPORTED on a device that is not sm_103):
+ *   the fp32 scores and top-k indices live in a 64 MiB static
  *   __device__ array inside the library, which every GPU that loads the library
  *   holds until the process exits.  No cudaMalloc/cudaFree or other allocating
  *   call is made.

@@ -78,11 +78,6 @@ smla_status_t check_device(DeviceInfo** out) {
   return SMLA_OK;
 }
 
-bool layout_ok(const smla_layout_t* l) {
-  return l != nullptr && l->block_size > 0 && l->n_layers > 0 && l->num_blocks > 0 && l->block_stride > 0 &&
-         l->d_latent > 0 && l->quant_tile > 0 && l->d_index > 0;
-}
-
 // Query tokens per group so the fp32 score scratch stays within kScoreBudget.
 int query_group(int n_tokens, int64_t stride) {
   int64_t g = static_cast<int64_t>(kScoreBudget / (static_cast<size_t>(stride) * 4));
@@ -107,6 +102,46 @@ unsigned* device_error_word() {
 int device_sm_count() {
   DeviceInfo* d = current_device();
   return d && d->sms > 0 ? d->sms : 1;
+}
+
+smla_status_t checked_device(unsigned** err) {
+  DeviceInfo* d = nullptr;
+  const smla_status_t st = check_device(&d);
+  if (st == SMLA_OK) *err = d->err;
+  return st;
+}
+
+bool layout_ok(const smla_layout_t* l) {
+  if (l == nullptr) return false;
+  smla_layout_t ref;
+  if (smla_layout_init(&ref, l->block_size, l->n_layers, l->d_latent, l->d_rope, l->quant_tile, l->d_index,
+                       l->num_blocks) != SMLA_OK)
+    return false;
+  return l->n_scales == ref.n_scales && l->rec_bytes == ref.rec_bytes && l->rec_stride == ref.rec_stride &&
+         l->rec_off == ref.rec_off && l->idx_key_off == ref.idx_key_off && l->idx_scale_off == ref.idx_scale_off &&
+         l->layer_stride == ref.layer_stride && l->block_stride == ref.block_stride;
+}
+
+smla_status_t check_step(const StepArgs& a) {
+  const smla_layout_t* layout = a.layout;
+  const smla_params_t* params = a.params;
+  if (!layout_ok(layout) || !params || a.layer < 0 || a.layer >= layout->n_layers || a.batch <= 0 ||
+      a.n_tokens < 0 || a.max_q <= 0 || a.max_ctx <= 0 || params->top_k <= 0 || params->n_heads <= 0 ||
+      params->n_idx_heads <= 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (a.n_tokens == 0) return SMLA_OK;
+  if (!a.pool || !a.q || (layout->d_rope > 0 && !a.q_pe) || !a.q_idx || !a.w || !a.block_table || !a.seq_lens ||
+      !a.query_start_loc || !a.out || !a.lse || a.bt_stride <= 0 ||
+      static_cast<int64_t>(a.bt_stride) * layout->block_size < a.max_ctx)
+    return SMLA_ERR_INVALID_ARG;
+  if (a.slot_mapping != nullptr &&
+      (!a.new_latent || !a.new_idx_k || !a.new_idx_scale || (layout->d_rope > 0 && !a.new_rope)))
+    return SMLA_ERR_INVALID_ARG;
+  const KernelLayout L = kernel_layout(*layout);
+  if ((a.slot_mapping != nullptr && !store_shape_supported(L)) || !index_shape_supported(L, params->n_idx_heads) ||
+      !attend_shape_supported(L, params->n_heads))
+    return SMLA_ERR_UNSUPPORTED;
+  return SMLA_OK;
 }
 
 }  // namespace smla
@@ -278,22 +313,20 @@ smla_status_t smla_decode(const smla_layout_t* layout, const smla_params_t* para
                           const int32_t* seq_lens, const int32_t* query_start_loc, int batch, int n_tokens,
                           int max_q, int max_ctx, void* out, float* lse, int32_t* topk_idx_out, void* workspace,
                           size_t workspace_bytes, void* stream) {
-  if (!layout_ok(layout) || !params || layer < 0 || layer >= layout->n_layers || batch <= 0 || n_tokens < 0 ||
-      max_q <= 0 || max_ctx <= 0 || params->top_k <= 0)
+  const StepArgs args{layout,   params,     pool,    layer,   new_latent, new_rope,  new_idx_k,       new_idx_scale,
+                      slot_mapping, q,      q_pe,    q_idx,   w,          block_table, bt_stride,     seq_lens,
+                      query_start_loc, batch, n_tokens, max_q, max_ctx,   out,       lse};
+  smla_status_t st = check_step(args);
+  if (st != SMLA_OK || n_tokens == 0) return st;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
+      workspace_bytes < smla_workspace_size(layout, params, n_tokens, max_ctx))
     return SMLA_ERR_INVALID_ARG;
-  if (n_tokens == 0) return SMLA_OK;
-  if (!pool || !q || !q_idx || !w || !block_table || !seq_lens || !query_start_loc || !out || !lse || !workspace ||
-      (reinterpret_cast<uintptr_t>(workspace) & 255) != 0 ||
-      static_cast<int64_t>(bt_stride) * layout->block_size < max_ctx)
-    return SMLA_ERR_INVALID_ARG;
-  if (workspace_bytes < smla_workspace_size(layout, params, n_tokens, max_ctx)) return SMLA_ERR_INVALID_ARG;
   DeviceInfo* d;
-  smla_status_t st = check_device(&d);
+  st = check_device(&d);
   if (st != SMLA_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const KernelLayout L = kernel_layout(*layout);
   if (slot_mapping != nullptr) {
-    if (!new_latent || !new_idx_k || !new_idx_scale || (layout->d_rope > 0 && !new_rope)) return SMLA_ERR_INVALID_ARG;
     st = launch_kvpack_store(L, pool, layer, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping, n_tokens,
                              s, d->err);
     if (st != SMLA_OK) return st;

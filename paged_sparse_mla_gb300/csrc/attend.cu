@@ -87,6 +87,7 @@ struct AttnArgs {
   const int32_t* topk;  // rows relative to tok_begin
   const int32_t* block_table;
   int bt_stride;
+  int64_t max_pos;  // bt_stride * block_size: positions at or past it have no block-table entry
   const int32_t* qsl;
   int batch, tok_begin, n_rows;
   __nv_bfloat16* out;
@@ -400,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int e = (tb + tile) * kTile + ptid;
         return (ptid < kTile && tile < ntiles && e < A.top_k) ? __ldg(idx + e) : -1;
       };
-      const auto block_of = [&](int j) -> int { return j >= 0 ? __ldg(bt + j / L.block_size) : -1; };
+      // a position past the sequence's block-table row reads no entry; rec_of latches it as a bad index
+      const auto block_of = [&](int j) -> int { return j >= 0 && j < A.max_pos ? __ldg(bt + j / L.block_size) : -1; };
       if (ptid < kTile) {
         const int j0 = entry(0), j1 = entry(1);
         const int b0 = block_of(j0), b1 = block_of(j1);
@@ -915,6 +917,11 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
 
 }  // namespace
 
+// Up to 64 heads, rope of at most 64 dims, a latent of 64 or 512 dims.
+bool attend_shape_supported(const KernelLayout& L, int n_heads) {
+  return n_heads > 0 && n_heads <= kHeads && L.d_rope <= 64 && (L.d_latent == 64 || L.d_latent == 512);
+}
+
 smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float softmax_scale, const void* pool,
                             int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
                             const int32_t* block_table, int bt_stride, const int32_t* query_start_loc, int batch,
@@ -922,7 +929,7 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
                             const void* host_records, const int32_t* host_block_map, int64_t n_host_blocks,
                             void* split_ws, size_t split_ws_bytes) {
   if (tok_end <= tok_begin) return SMLA_OK;
-  if (n_heads > kHeads || L.d_rope > 64 || L.d_latent % 64 != 0) return SMLA_ERR_UNSUPPORTED;
+  if (!attend_shape_supported(L, n_heads)) return SMLA_ERR_UNSUPPORTED;
   // Fewer rows than SMs: each row's tiles are split over up to sms / rows CTAs (one wave of
   // units), as far as the caller's scratch holds the partials.
   const int n_rows = tok_end - tok_begin;
@@ -945,6 +952,7 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
   A.topk = topk_idx;
   A.block_table = block_table;
   A.bt_stride = bt_stride;
+  A.max_pos = static_cast<int64_t>(bt_stride) * L.block_size;
   A.qsl = query_start_loc;
   A.batch = batch;
   A.tok_begin = tok_begin;

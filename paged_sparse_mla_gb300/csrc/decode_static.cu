@@ -67,29 +67,27 @@ extern "C" smla_status_t smla_decode_static(const smla_layout_t* layout, const s
                                             int bt_stride, const int32_t* seq_lens, const int32_t* query_start_loc,
                                             int batch, int n_tokens, int max_q, int max_ctx, void* out, float* lse,
                                             int32_t* topk_idx_out, void* stream) {
-  if (layout == nullptr || params == nullptr || layout->block_size <= 0 || layout->num_blocks <= 0 ||
-      layer < 0 || layer >= layout->n_layers || batch <= 0 || n_tokens < 0 || max_q <= 0 || max_ctx <= 0 ||
-      params->top_k <= 0)
-    return SMLA_ERR_INVALID_ARG;
-  if (n_tokens == 0) return SMLA_OK;
-  if (!pool || !q || !q_idx || !w || !block_table || !seq_lens || !query_start_loc || !out || !lse ||
-      static_cast<int64_t>(bt_stride) * layout->block_size < max_ctx)
-    return SMLA_ERR_INVALID_ARG;
+  // the same argument checks, in the same order, as smla_decode
+  const StepArgs args{layout,   params,     pool,    layer,   new_latent, new_rope,  new_idx_k,       new_idx_scale,
+                      slot_mapping, q,      q_pe,    q_idx,   w,          block_table, bt_stride,     seq_lens,
+                      query_start_loc, batch, n_tokens, max_q, max_ctx,   out,       lse};
+  smla_status_t st = check_step(args);
+  if (st != SMLA_OK || n_tokens == 0) return st;
   // Query tokens go in groups whose scores and indices fit the static scratch.
   const int64_t stride = round_up_static(max_ctx, 4);
   const int64_t per_token = stride * 4 + static_cast<int64_t>(params->top_k) * 4;
   int64_t g = static_cast<int64_t>(kStaticScratchBytes - 512) / per_token;
   if (g < 1) return SMLA_ERR_SCRATCH_LIMIT;  // one token's score row and indices exceed the scratch
+  unsigned* err = nullptr;
+  st = checked_device(&err);  // sm_103 device (as smla_decode), and its error word
+  if (st != SMLA_OK) return st;
   g = wave_aligned_group(g, n_tokens);
   uint8_t* scratch = nullptr;
-  smla_status_t st = static_scratch(&scratch);
+  st = static_scratch(&scratch);
   if (st != SMLA_OK) return st;
-  unsigned* err = device_error_word();
-  if (err == nullptr) return SMLA_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const KernelLayout L = kernel_layout(*layout);
   if (slot_mapping != nullptr) {
-    if (!new_latent || !new_idx_k || !new_idx_scale || (layout->d_rope > 0 && !new_rope)) return SMLA_ERR_INVALID_ARG;
     st = launch_kvpack_store(L, pool, layer, new_latent, new_rope, new_idx_k, new_idx_scale, slot_mapping, n_tokens, s,
                              err);
     if (st != SMLA_OK) return st;

@@ -561,12 +561,19 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
+// Shapes built into the library: (indexer heads, key dims, block size).
+bool index_shape_supported(const KernelLayout& L, int n_idx_heads) {
+  return (n_idx_heads == 64 && L.d_index == 128 && (L.block_size == 64 || L.block_size == 16)) ||
+         (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16);
+}
+
 smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const void* pool, int layer,
                                   const uint8_t* q_idx, const float* w, const int32_t* block_table, int bt_stride,
                                   const int32_t* seq_lens, const int32_t* query_start_loc, int batch, int tok_begin,
                                   int tok_end, int max_q, int max_ctx, float* scores, int64_t scores_stride,
                                   cudaStream_t stream, unsigned* err) {
   if (tok_end <= tok_begin || max_ctx <= 0) return SMLA_OK;
+  if (!index_shape_supported(L, n_idx_heads)) return SMLA_ERR_UNSUPPORTED;
   IdxArgs A;
   A.L = L;
   A.n_idx_heads = n_idx_heads;
@@ -592,7 +599,6 @@ smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const 
   const int grid = static_cast<int>(items < sms ? items : sms);
   // Query rows are addressed by absolute token (token t -> rows t*heads ..), so the map spans every
   // token below tok_end; the box of a group near the end reads past it as zeros.
-  // Shapes built into the library: (indexer heads, key dims, block size).
   if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 64)
     return launch_shape<64, 128, 64>(A, q_idx, tok_end, grid, stream);
   if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 16)

@@ -45,6 +45,44 @@ EncodeTiledFn encode_tiled();
 // Device error word (defined in api.cu); launchers receive its address.
 unsigned* device_error_word();
 int device_sm_count();
+// The current device's error word, after checking that the device is sm_103 (SMLA_ERR_UNSUPPORTED
+// otherwise; SMLA_ERR_CUDA if the device or the word's address cannot be read).
+smla_status_t checked_device(unsigned** err);
+
+// A layout is accepted only as smla_layout_init produced it: its shape fields pass that call's
+// checks and every derived field (record size, region offsets, strides) equals what it computes.
+bool layout_ok(const smla_layout_t* l);
+
+// Shapes compiled into the kernels; the entry points refuse others with SMLA_ERR_UNSUPPORTED
+// before anything is enqueued.
+bool store_shape_supported(const KernelLayout& L);
+bool index_shape_supported(const KernelLayout& L, int n_idx_heads);
+bool attend_shape_supported(const KernelLayout& L, int n_heads);
+
+// Arguments of one fused step (smla_decode and smla_decode_static take the same ones apart from
+// the scratch), checked by check_step() in the same order for both.
+struct StepArgs {
+  const smla_layout_t* layout;
+  const smla_params_t* params;
+  void* pool;
+  int layer;
+  const void *new_latent, *new_rope;
+  const uint8_t* new_idx_k;
+  const float* new_idx_scale;
+  const int64_t* slot_mapping;
+  const void *q, *q_pe;
+  const uint8_t* q_idx;
+  const float* w;
+  const int32_t* block_table;
+  int bt_stride;
+  const int32_t *seq_lens, *query_start_loc;
+  int batch, n_tokens, max_q, max_ctx;
+  void* out;
+  float* lse;
+};
+// SMLA_ERR_INVALID_ARG for a bad pointer, size or layout, SMLA_ERR_UNSUPPORTED for a shape the
+// kernels do not build, else SMLA_OK (also for n_tokens == 0, which enqueues nothing).
+smla_status_t check_step(const StepArgs& a);
 // Launch attributes (shared-memory opt-in, occupancy) belong to a device: launchers keep
 // them per device, in tables of kMaxDeviceSlots entries indexed by current_device_index().
 constexpr int kMaxDeviceSlots = 64;

@@ -70,10 +70,16 @@ __global__ void __launch_bounds__(256) kvpack_store_kernel(KernelLayout L, uint8
   }
 }
 
+bool store_shape_supported(const KernelLayout& L) {
+  const int e = L.d_latent / 32;  // latent elements per lane
+  return L.d_latent % 32 == 0 && (e == 2 || e == 4 || e == 8 || e == 16);
+}
+
 smla_status_t launch_kvpack_store(const KernelLayout& L, void* pool, int layer, const void* latent,
                                   const void* rope, const uint8_t* idx_k, const float* idx_scale,
                                   const int64_t* slot_mapping, int n_tokens, cudaStream_t stream, unsigned* err) {
   if (n_tokens == 0) return SMLA_OK;
+  if (!store_shape_supported(L)) return SMLA_ERR_UNSUPPORTED;
   const int threads = 256;
   const int blocks = (n_tokens * 32 + threads - 1) / threads;
   auto* pl = static_cast<uint8_t*>(pool);

@@ -43,6 +43,38 @@ int main(void) {
   CHECK(10, kvpack_store(&lay, NULL, 0, NULL, NULL, NULL, NULL, NULL, 0, NULL) == SMLA_OK);
   CHECK(11, smla_topk(&prm, NULL, 0, NULL, NULL, 1, 4, NULL, NULL, 0, NULL) == SMLA_ERR_INVALID_ARG);
 
+  {
+    /* The two fused entry points refuse the same malformed arguments with the same status,
+     * before any device work.  The dummy pointers are never dereferenced on the host. */
+    void* p = (void*)(uintptr_t)4096;
+    const uint8_t* u8 = (const uint8_t*)p;
+    const float* f32 = (const float*)p;
+    const int32_t* i32 = (const int32_t*)p;
+    const int64_t* i64 = (const int64_t*)p;
+    smla_layout_t bad;
+    smla_params_t bp;
+    int c;
+    for (c = 0; c < 6; ++c) {
+      smla_status_t want = SMLA_ERR_INVALID_ARG;
+      const void* q_pe = p;
+      bad = lay;
+      bp = prm;
+      if (c == 0) bad.quant_tile = 0;        /* not a layout smla_layout_init makes */
+      if (c == 1) bad.block_stride = 0;
+      if (c == 2) bad.idx_key_off += 16;
+      if (c == 3) q_pe = NULL;               /* d_rope > 0 needs q_pe */
+      if (c == 4) bp.n_heads = 0;
+      if (c == 5) {
+        bp.n_idx_heads = 3;                  /* a shape the kernels do not build */
+        want = SMLA_ERR_UNSUPPORTED;
+      }
+      CHECK(20 + c, smla_decode(&bad, &bp, p, 0, p, p, u8, f32, i64, p, q_pe, u8, f32, i32, 16, i32, i32, 1, 1, 1,
+                                1000, p, (float*)p, NULL, p, (size_t)1 << 30, NULL) == want);
+      CHECK(30 + c, smla_decode_static(&bad, &bp, p, 0, p, p, u8, f32, i64, p, q_pe, u8, f32, i32, 16, i32, i32, 1,
+                                       1, 1, 1000, p, (float*)p, NULL, NULL) == want);
+    }
+  }
+
   CHECK(12, strcmp(smla_status_string(SMLA_ERR_BAD_INDEX), "SMLA_ERR_BAD_INDEX") == 0);
   CHECK(13, strcmp(smla_status_string(SMLA_ERR_SCRATCH_LIMIT), "SMLA_ERR_SCRATCH_LIMIT") == 0);
   CHECK(14, smla_version() >= 100);

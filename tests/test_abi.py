@@ -83,6 +83,48 @@ def test_host_side_argument_checks(lib):
     assert lib.smla_version() >= 100
 
 
+@pytest.mark.parametrize("field,delta", [("idx_key_off", 16), ("block_stride", -256), ("rec_stride", 16),
+                                         ("quant_tile", -128), ("layer_stride", 256), ("n_scales", 1)])
+def test_layouts_not_made_by_layout_init_are_refused_everywhere(lib, field, delta):
+    """Every entry point that takes a layout refuses one whose fields differ from smla_layout_init's,
+    before any device work; the two fused entry points answer alike."""
+    lay = smla.layout_init(64, 1, 512, 64, 128, 128, 10)
+    setattr(lay, field, getattr(lay, field) + delta)
+    prm = smla.make_params(64, 64, 2048, 1 / 24)
+    L, P = ctypes.byref(lay), ctypes.byref(prm)
+    p = ctypes.c_void_p(4096)                                    # never dereferenced on the host
+    assert lib.smla_workspace_size(L, P, 4, 1000) == 0
+    assert lib.smla_attend_workspace_size(L, P, 4) == 0
+    assert lib.kvpack_store(L, p, 0, p, p, p, p, p, 1, None) == 1
+    assert lib.smla_index_scores(L, P, p, 0, p, p, p, 16, p, p, 1, 1, 1, 1000, p, 1000, None) == 1
+    assert lib.smla_attend(L, P, p, 0, p, p, p, p, 16, p, 1, 1, p, p, None, 0, None) == 1
+    step = (p, 0, p, p, p, p, p, p, p, p, p, p, 16, p, p, 1, 1, 1, 1000, p, p, None)
+    assert lib.smla_decode(L, P, *step, p, 1 << 30, None) == 1
+    assert lib.smla_decode_static(L, P, *step, None) == 1
+
+
+@pytest.mark.parametrize("case", ["q_pe", "n_heads", "n_idx_heads", "top_k", "unbuilt_idx_heads", "unbuilt_heads"])
+def test_fused_entry_points_refuse_the_same_arguments(lib, case):
+    """smla_decode and smla_decode_static apply the same checks and return the same status, with
+    nothing enqueued (these run without a GPU)."""
+    lay = smla.layout_init(64, 1, 512, 64, 128, 128, 10)
+    prm = smla.make_params(64, 64, 2048, 1 / 24)
+    p = ctypes.c_void_p(4096)
+    q_pe = None if case == "q_pe" else p
+    want = 1
+    if case in ("n_heads", "n_idx_heads", "top_k"):
+        setattr(prm, case, 0)
+    if case == "unbuilt_idx_heads":
+        prm.n_idx_heads, want = 32, 2
+    if case == "unbuilt_heads":
+        prm.n_heads, want = 65, 2
+    L, P = ctypes.byref(lay), ctypes.byref(prm)
+    step = (p, 0, p, p, p, p, p, p, q_pe, p, p, p, 16, p, p, 1, 1, 1, 1000, p, p, None)
+    a = lib.smla_decode(L, P, *step, p, 1 << 30, None)
+    b = lib.smla_decode_static(L, P, *step, None)
+    assert a == b == want
+
+
 def test_header_is_c99_and_the_library_links_from_c(lib, tmp_path):
     """A plain C caller (tests/c/abi_host_check.c) compiles against include/smla.h with gcc -std=c99
     -pedantic -Werror, links libsmla.so and gets the documented host-side answers."""

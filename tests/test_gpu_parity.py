@@ -203,6 +203,27 @@ def test_bad_block_id_is_reported_not_faulted():
     assert G.smla.smla_get_last_error() == 0        # cleared by the read
 
 
+def test_position_past_the_block_table_row_is_reported_not_read():
+    """A caller-supplied top-k entry at or beyond bt_stride * block_size has no block-table entry:
+    the attention latches SMLA_ERR_BAD_INDEX and treats its record as zeros, and the other rows
+    are unaffected."""
+    g = G.cuda_wl(make_config(1))
+    lay, prm = G.gpu_layout(g), G.gpu_params(g)
+    pool = G.gpu_pool(g, lay)
+    base = G.run_stages(g, pool, lay, prm, store=False)
+    assert base["err"] == 0
+    topk = torch.as_tensor(base["topk"], device="cuda")
+    bad = topk.clone()
+    bad[0, 0] = g.block_table.shape[1] * g.dims.block_size + 3      # past the last block-table column
+    T, d = g.n_tokens, g.dims
+    out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
+    smla.smla_attend(lay, prm, pool, 0, g.q, g.q_pe, bad, g.block_table, g.query_start_loc, out, lse)
+    assert smla.smla_get_last_error() == 4                          # SMLA_ERR_BAD_INDEX
+    o = out.float().cpu().numpy()
+    assert np.array_equal(o[1:], base["out"][1:])                   # other rows untouched
+
+
 def test_wait_that_never_completes_times_out_and_context_survives():
     """A bounded wait on an mbarrier nothing arrives at gives up, reports SMLA_ERR_TIMEOUT and returns."""
     import time
