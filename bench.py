@@ -854,6 +854,77 @@ def run_hisparse(args):
     print(json.dumps(line))
 
 
+def run_topk_rows(args):
+    """--topk-rows: smla_topk alone on score rows of the workload's query tokens (their visible lengths),
+    drawn two ways: i.i.d. integer scores (the sampled threshold works: one streaming pass) and the same
+    rows with the highest scores clustered on the most recent 6,000 positions (as recent turns would be),
+    which overflows one warp's candidate list and takes the exact radix-select fallback over the whole
+    row.  Prints one JSON line with both times."""
+    import paged_sparse_mla_gb300 as smla
+    from paged_sparse_mla_gb300 import build_lib
+    from paged_sparse_mla_gb300.workloads import make_config
+
+    torch.cuda.set_device(0)
+    build_lib.build()
+    smla.lib()
+    wl = make_config(args.workload, device="cuda", scale=args.scale)
+    d = wl.dims
+    qsl = wl.query_start_loc.cpu().numpy()
+    lens = wl.seq_lens.cpu().numpy()
+    wl.slot_latent = wl.slot_rope = wl.slot_idx_k = wl.slot_idx_s = None
+    T = int(qsl[-1])
+    seq = np.searchsorted(qsl, np.arange(T), side="right") - 1
+    n_vis = lens[seq] - (qsl[seq + 1] - qsl[seq]) + (np.arange(T) - qsl[seq]) + 1
+    stride = (int(n_vis.max()) + 3) // 4 * 4
+    gen = torch.Generator(device="cuda").manual_seed(77)
+    base = (torch.randint(-60, 61, (T, stride), generator=gen, device="cuda").float() * 0.25)
+    clustered = base.clone()
+    cols = torch.arange(stride, device="cuda")[None, :]
+    nv = torch.as_tensor(n_vis, device="cuda")[:, None]
+    hot = (cols >= nv - 6000) & (cols < nv)
+    clustered[hot] = 100.0 + torch.randint(0, 40, (int(hot.sum()),), generator=gen, device="cuda").float()
+    prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
+    sl = wl.seq_lens
+    qs = wl.query_start_loc
+    out = torch.empty((T, d.top_k), dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def timed(scores):
+        fn = lambda: smla.smla_topk(prm, scores, sl, qs, out, stream=stream)
+        for _ in range(args.warmup):
+            fn()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(args.steps):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / args.steps
+
+    clocks = ClockSampler(0, args.clocks_csv)
+    time.sleep(0.3)
+    clocks.start_window()
+    ms_fast = timed(base)
+    ms_slow = timed(clustered)
+    clocks.end_window()
+    clk = clocks.stop()
+    if smla.smla_get_last_error() != 0:
+        raise RuntimeError("device error in the timed region")
+    line = {
+        "metric": "top-k select time per launch: i.i.d. scores vs scores clustered on recent positions",
+        "value": round(ms_slow, 4), "unit": "ms", "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(ms_slow, 4), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp32 scores, int32 positions", "data": "synthetic",
+        "config": {"workload": wl.name, "rows": T, "top_k": d.top_k, "mean_visible": round(float(n_vis.mean()), 1),
+                   "max_visible": int(n_vis.max()), "cluster": "highest scores on the last 6,000 visible positions"},
+        "iid_rows_ms": round(ms_fast, 4), "clustered_rows_ms": round(ms_slow, 4),
+        "score_bytes_per_launch": int(n_vis.sum()) * 4,
+        "clocks": clk,
+    }
+    print(json.dumps(line))
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -871,6 +942,8 @@ def main():
                     help="split-context arm: N round-robin token shards on one GPU (decode workloads 2 and 4)")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="shrink context lengths (profiler captures of a smaller case; not a bench line)")
+    ap.add_argument("--topk-rows", action="store_true",
+                    help="top-k arm: smla_topk alone on i.i.d. and on clustered score rows of the workload's shape")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -880,6 +953,8 @@ def main():
         run_dcp(args)
     elif args.host_frac > 0:
         run_hisparse(args)
+    elif args.topk_rows:
+        run_topk_rows(args)
     else:
         run_gpu(args)
 

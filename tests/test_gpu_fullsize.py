@@ -7,7 +7,10 @@ Indexer scores of those rows are compared bit for bit, top-k exactly,
 attention within the stated tolerance.  Every other row's selection is checked
 against its own GPU score row with the exact top-k characterisation of
 tests/topk_properties.py (count, order, range, threshold, ties), which holds
-at any size.
+at any size.  Once every selection is shown exact that way, every row's
+attention output and lse are compared with oracle.sparse_attend over that
+selection, on an oracle pool that holds the selected records (written by the
+oracle's own store from the workload's inputs).
 """
 import numpy as np
 import pytest
@@ -77,3 +80,26 @@ def test_full_size_sampled_rows(cfg):
             assert np.array_equal(G.canon(got), G.canon(ref[t]["scores"])), f"config {cfg} scores row {t}"
             assert np.array_equal(res["topk"][t], ref[t]["topk"]), f"config {cfg} topk row {t}"
             G.assert_attention_close(res["out"][t], res["lse"][t], ref[t]["out"], ref[t]["lse"], f"config {cfg} row {t}")
+    _check_every_row_attention(wl, lo, res, seqs, f"config {cfg}")
+
+
+def _check_every_row_attention(wl, lo, res, seqs, what):
+    """Every row's out/lse against oracle.sparse_attend over the row's (property-checked) selection."""
+    bs = wl.dims.block_size
+    bt = npy(wl.block_table)
+    topk = res["topk"]
+    rows = np.repeat(np.asarray(seqs, np.int64)[:, None], topk.shape[1], axis=1)
+    sel = topk >= 0
+    slots = np.unique(bt[rows[sel], topk[sel] // bs].astype(np.int64) * bs + topk[sel] % bs)
+    new_slots = npy(wl.slot_mapping)
+    ref_pool = oracle_pool(wl, slots=np.setdiff1d(slots, new_slots))
+    oracle.kvpack_store(lo, ref_pool, 0, bits(wl.new_latent), bits(wl.new_rope), npy(wl.new_idx_k),
+                        npy(wl.new_idx_s), new_slots)
+    q, q_pe = bits(wl.q), bits(wl.q_pe)
+    out_ref = np.empty(res["out"].shape, np.float64)
+    lse_ref = np.empty(res["lse"].shape, np.float64)
+    for t in range(wl.n_tokens):
+        out_ref[t], lse_ref[t] = oracle.sparse_attend(lo, ref_pool, 0, oracle.bf16_bits_to_f64(q[t]),
+                                                      oracle.bf16_bits_to_f64(q_pe[t]), topk[t], bt[seqs[t]],
+                                                      wl.dims.softmax_scale)
+    G.assert_attention_close(res["out"], res["lse"], out_ref, lse_ref, f"{what}, every row")
