@@ -24,6 +24,9 @@ Sources, abbreviated in the docstrings below:
   "Config and numbers" (MTP3; FP8 KV), "How to try" (sparse_mla_force_mqa:
   prompts inside the top-k still take the sparse MQA kernel; FP8 KV cache).
 * [OCP-FP8] -- the OCP 8-bit floating point specification (E4M3 format).
+* [OCP-MX]  -- the OCP Microscaling Formats (MX) specification, for its FP4
+  E2M1 element type, the reading taken for FP4 indexer keys ([AgentX "Hybrid
+  KV cache management"] names an FP4 indexer but no format).
 
 ``oracle.dcp`` states the split-context form (token shards, candidate merge,
 log-sum-exp merge of partial outputs) of [AgentX "Kimi K3"] DCP.
@@ -38,6 +41,7 @@ Pins (tests that tie this oracle to something other than itself) live in
 """
 
 from .fp8 import e4m3_decode, e4m3_encode, E4M3_MAX
+from .fp4 import e2m1_decode, e2m1_encode, e2m1_pack, e2m1_unpack, E2M1_MAX
 from .layout import PoolLayout
 from .store import kvpack_store, read_record, read_index_key
 from .indexer import index_scores, index_scores_row, query_positions, context_slots
@@ -48,7 +52,8 @@ from .store import bf16_bits_to_f64, quantize_latent
 from . import dcp
 
 __all__ = [
-    "e4m3_decode", "e4m3_encode", "E4M3_MAX", "PoolLayout", "kvpack_store",
+    "e4m3_decode", "e4m3_encode", "E4M3_MAX", "e2m1_decode", "e2m1_encode", "e2m1_pack", "e2m1_unpack",
+    "E2M1_MAX", "PoolLayout", "kvpack_store",
     "read_record", "read_index_key", "index_scores", "index_scores_row",
     "query_positions", "context_slots", "topk_select", "attend", "sparse_attend",
     "dense_attend", "decode_step", "bf16_bits_to_f64", "quantize_latent", "dcp",

@@ -7,9 +7,11 @@ top-k selection per token.  [GLM-5.3 "What is new"]: the indexer chooses
 reading (score function): for query token t and every cached position j it
 may see,
     I[t, j] = s_I[j] * sum_h  w[t, h] * ReLU( sum_d qI[t, h, d] * kI[j, d] )
-with qI, kI decoded E4M3 values, one indexer key per cached token shared by all
-indexer heads, w the per-(token, head) weight and s_I[j] the key's fp32 scale.
-Accumulated in float64 and rounded once to float32.
+with qI decoded E4M3 values, kI decoded E4M3 values (or FP4 E2M1 values for a
+layout with FP4 keys, [AgentX "Hybrid KV cache management"]), one indexer key
+per cached token shared by all indexer heads, w the per-(token, head) weight
+and s_I[j] the key's fp32 scale.  Accumulated in float64 and rounded once to
+float32.
 
 reading (query positions): ``seq_lens[b]`` counts this step's tokens, which
 are stored before the scores are taken; query i of the n_q tokens of sequence b

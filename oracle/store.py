@@ -10,8 +10,9 @@ tiles of ``quant_tile`` elements.  Per tile:
     scale = fp32(amax / 448)                 (one IEEE fp32 division, RNE)
     scale = 1.0 if scale == 0
     code  = e4m3_rne_satfinite(fp32(x / scale))
-The rope part (bf16) and the caller-supplied indexer key (e4m3 bytes) and
-indexer scale (fp32) are copied verbatim.  ``slot_mapping[t] == -1`` skips
+The rope part (bf16) and the caller-supplied indexer key (e4m3 bytes, or
+packed e2m1 bytes for a layout with FP4 keys) and indexer scale (fp32) are
+copied verbatim.  ``slot_mapping[t] == -1`` skips
 token t.  Dequantisation of a code is fp32(decode(code) * scale).
 
 fp32 division and multiplication are evaluated in float64 and rounded once to
@@ -21,6 +22,7 @@ correctly rounded p-bit result (no double-rounding error), and float64 has 53.
 
 import numpy as np
 
+from .fp4 import e2m1_decode, e2m1_unpack
 from .fp8 import e4m3_decode, e4m3_encode, E4M3_MAX
 from .layout import PoolLayout
 
@@ -51,7 +53,7 @@ def _offsets(layout: PoolLayout, slots, layer: int, region: str) -> np.ndarray:
     if region == "record":
         return base + layout.rec_off + off * layout.rec_stride
     if region == "key":
-        return base + layout.idx_key_off + off * layout.d_index
+        return base + layout.idx_key_off + off * layout.key_bytes
     return base + layout.idx_scale_off + off * 4
 
 
@@ -65,7 +67,7 @@ def kvpack_store(layout: PoolLayout, pool: np.ndarray, layer: int, latent_bits, 
     idx_k = np.asarray(idx_k, dtype=np.uint8)[keep]
     idx_scale = np.ascontiguousarray(np.asarray(idx_scale, dtype=np.float32)[keep])
     slots = slots[keep]
-    d_l, n_s, d_r, d_i = layout.d_latent, layout.n_scales, layout.d_rope, layout.d_index
+    d_l, n_s, d_r, d_i = layout.d_latent, layout.n_scales, layout.d_rope, layout.key_bytes
     rec = _offsets(layout, slots, layer, "record")[:, None]
     pool[rec + np.arange(d_l)] = codes
     pool[rec + d_l + np.arange(4 * n_s)] = np.ascontiguousarray(scales).view(np.uint8).reshape(-1, 4 * n_s)
@@ -89,9 +91,10 @@ def read_record(layout: PoolLayout, pool: np.ndarray, layer: int, slots):
 
 
 def read_index_key(layout: PoolLayout, pool: np.ndarray, layer: int, slots):
-    """Indexer keys (decoded e4m3, float64) [n, D_I] and their fp32 scales [n] (float64)."""
+    """Indexer keys (decoded e4m3 or e2m1, float64) [n, D_I] and their fp32 scales [n] (float64)."""
     key = _offsets(layout, slots, layer, "key")[:, None]
-    keys = e4m3_decode(pool[key + np.arange(layout.d_index)])
+    raw = pool[key + np.arange(layout.key_bytes)]
+    keys = e4m3_decode(raw) if layout.key_format == "e4m3" else e2m1_decode(e2m1_unpack(raw))
     sc = _offsets(layout, slots, layer, "scale")[:, None]
     scales = np.ascontiguousarray(pool[sc + np.arange(4)]).view(np.float32)[:, 0]
     return keys, scales.astype(np.float64)

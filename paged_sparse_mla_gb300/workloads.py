@@ -13,7 +13,10 @@ parent context, MTP3 decode, chunked prefill on a cached prefix):
   stored as E4M3 (exact for such integers);
 * indexer head weights drawn uniformly from {0.25, 0.5, 1};
 * indexer key scales 1.0 (tests also use powers of two);
-* physical block ids are a random permutation of the pool.
+* physical block ids are a random permutation of the pool;
+* with FP4 indexer keys (``key_format="e2m1"``), every key element is a
+  uniformly drawn 4-bit E2M1 code (all sixteen, so the values 0, +-0.5, +-1,
+  +-1.5, +-2, +-3, +-4, +-6), two codes packed per byte, low nibble first.
 
 Five named shapes (``make_config(i)``):
   1 tiny decode: 2 seqs x 1 query, ctx 256, bs 16, 8 shared prefix blocks,
@@ -25,9 +28,10 @@ Five named shapes (``make_config(i)``):
     (1 + Poisson(3) each) sharing >= 96% of their blocks.
   4 long-context decode: 8 seqs x 1 query, ctx 1,048,576.
   5 chunked prefill: 1 seq, 131,072 cached + 8,192 new query tokens.
+``make_config(i, key_format="e2m1")`` gives shapes 2-5 with FP4 indexer keys.
 """
 
-from dataclasses import dataclass, field
+from dataclasses import dataclass, field, replace
 import math
 
 import numpy as np
@@ -46,10 +50,15 @@ class Dims:
     block_size: int = 64
     n_layers: int = 1
     idx_range: int = 8
+    key_format: str = "e4m3"   # indexer keys: "e4m3" (one byte per element) or "e2m1" (packed FP4)
 
     @property
     def softmax_scale(self) -> float:
         return 1.0 / math.sqrt(self.d_latent + self.d_rope)
+
+    @property
+    def key_bytes(self) -> int:
+        return self.d_index if self.key_format == "e4m3" else self.d_index // 2
 
 
 TINY = Dims(n_heads=8, d_latent=64, d_rope=16, quant_tile=64, n_idx_heads=4, d_index=32,
@@ -69,11 +78,11 @@ class Workload:
     cached_slots: torch.Tensor       # int64 [Nc], slots holding earlier tokens (deduplicated)
     slot_latent: torch.Tensor        # bf16 [num_blocks * bs, D_L]: value of each physical slot
     slot_rope: torch.Tensor          # bf16 [num_blocks * bs, D_R]
-    slot_idx_k: torch.Tensor         # uint8 (E4M3) [num_blocks * bs, D_I]
+    slot_idx_k: torch.Tensor         # uint8 [num_blocks * bs, key_bytes] (E4M3, or packed E2M1)
     slot_idx_s: torch.Tensor         # fp32 [num_blocks * bs]
     new_latent: torch.Tensor         # bf16 [T, D_L]
     new_rope: torch.Tensor           # bf16 [T, D_R]
-    new_idx_k: torch.Tensor          # uint8 [T, D_I]
+    new_idx_k: torch.Tensor          # uint8 [T, key_bytes]
     new_idx_s: torch.Tensor          # fp32 [T]
     q: torch.Tensor                  # bf16 [T, H, D_L]
     q_pe: torch.Tensor               # bf16 [T, H, D_R]
@@ -101,6 +110,18 @@ def _gen(seed: int, device) -> torch.Generator:
 def _int_e4m3(shape, r: int, g, device) -> torch.Tensor:
     v = torch.randint(-r, r + 1, shape, generator=g, device=device, dtype=torch.int32)
     return v.to(torch.float32).to(torch.float8_e4m3fn).view(torch.uint8)
+
+
+def _packed_e2m1(shape, g, device) -> torch.Tensor:
+    """Uniform 4-bit codes, two per byte: [..., D] elements -> [..., D/2] bytes."""
+    *lead, d = shape
+    return torch.randint(0, 256, (*lead, d // 2), generator=g, device=device, dtype=torch.int32).to(torch.uint8)
+
+
+def _keys(shape, dims, g, device) -> torch.Tensor:
+    if dims.key_format == "e2m1":
+        return _packed_e2m1(shape, g, device)
+    return _int_e4m3(shape, dims.idx_range, g, device)
 
 
 def _normal_bf16(shape, g, device) -> torch.Tensor:
@@ -158,10 +179,10 @@ def build_workload(name: str, dims: Dims, ctx_lens, n_q, *, seed: int, device="c
     d = dims
     slot_latent = _normal_bf16((n_slots, d.d_latent), g, device)
     slot_rope = _normal_bf16((n_slots, d.d_rope), g, device)
-    slot_idx_k = _int_e4m3((n_slots, d.d_index), r, g, device)
+    slot_idx_k = _keys((n_slots, d.d_index), d, g, device)
     new_latent = _normal_bf16((t, d.d_latent), g, device)
     new_rope = _normal_bf16((t, d.d_rope), g, device)
-    new_idx_k = _int_e4m3((t, d.d_index), r, g, device)
+    new_idx_k = _keys((t, d.d_index), d, g, device)
     q = _normal_bf16((t, d.n_heads, d.d_latent), g, device)
     q_pe = _normal_bf16((t, d.n_heads, d.d_rope), g, device)
     q_idx = _int_e4m3((t, d.n_idx_heads, d.d_index), r, g, device)
@@ -224,8 +245,15 @@ def agentic_tree(seed: int, n_seqs: int = 64, n_parents: int = 13, n_q: int = 4,
     return lens, share
 
 
-def make_config(i: int, device="cpu", *, scale: float = 1.0) -> Workload:
-    """The five named shapes; ``scale`` < 1 shrinks context lengths (tests only)."""
+def make_config(i: int, device="cpu", *, scale: float = 1.0, key_format: str = "e4m3") -> Workload:
+    """The five named shapes; ``scale`` < 1 shrinks context lengths (tests only); ``key_format="e2m1"``
+    draws FP4 indexer keys for shapes 2-5 (names get a "-fp4keys" suffix)."""
+    if key_format not in ("e4m3", "e2m1"):
+        raise ValueError(f"unknown key format {key_format!r}")
+    if key_format == "e2m1" and i == 1:
+        raise ValueError("FP4 indexer keys are built for the 128-dim indexer of shapes 2-5")
+    full = FULL if key_format == "e4m3" else replace(FULL, key_format=key_format)
+    sfx = "" if key_format == "e4m3" else "-fp4keys"
     if i == 1:
         share = [(-1, 0), (0, 8)]
         return build_workload("tiny-decode", TINY, [256, 256], [1, 1], seed=0, device=device,
@@ -234,17 +262,17 @@ def make_config(i: int, device="cpu", *, scale: float = 1.0) -> Workload:
         rng = np.random.default_rng(1)
         lens = rng.integers(8192, 32768 + 1, size=32)
         lens = np.maximum((lens * scale).astype(np.int64), 2)
-        return build_workload("decode-b32-ctx8k-32k", FULL, lens, [1] * 32, seed=1, device=device)
+        return build_workload("decode-b32-ctx8k-32k" + sfx, full, lens, [1] * 32, seed=1, device=device)
     if i == 3:
         lens, share = agentic_tree(2, ctx_scale=scale)
-        return build_workload("agentic-mtp4-b64-ctx142k", FULL, lens, [4] * len(lens), seed=2,
+        return build_workload("agentic-mtp4-b64-ctx142k" + sfx, full, lens, [4] * len(lens), seed=2,
                               device=device, share=share)
     if i == 4:
         n = max(int(1_048_576 * scale), 2)
-        return build_workload("longctx-b8-ctx1m", FULL, [n] * 8, [1] * 8, seed=3, device=device)
+        return build_workload("longctx-b8-ctx1m" + sfx, full, [n] * 8, [1] * 8, seed=3, device=device)
     if i == 5:
         prefix, chunk = max(int(131_072 * scale), 1), max(int(8192 * scale), 1)
-        return build_workload("prefill-131k+8k", FULL, [prefix + chunk], [chunk], seed=4,
+        return build_workload("prefill-131k+8k" + sfx, full, [prefix + chunk], [chunk], seed=4,
                               device=device, slack_blocks=64)
     raise ValueError(f"unknown config {i}")
 

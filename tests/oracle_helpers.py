@@ -17,7 +17,7 @@ def npy(t: torch.Tensor) -> np.ndarray:
 def layout_of(wl) -> "oracle.PoolLayout":
     d = wl.dims
     return oracle.PoolLayout(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile,
-                             d.d_index, wl.num_blocks)
+                             d.d_index, wl.num_blocks, d.key_format)
 
 
 def oracle_pool(wl, layer: int = 0, slots=None, chunk: int = 1 << 17) -> np.ndarray:
