@@ -211,7 +211,7 @@ def accounting(wl, topk_host):
         blocks.update(bt[b, :nb].tolist())
         logical_keys += n
     uniq_keys = len(blocks) * bs
-    idx_rec = d.d_index + 4
+    idx_rec = d.key_bytes + 4          # cached key (E4M3, or packed E2M1) + its fp32 scale
     rec = ((d.d_latent + 4 * (d.d_latent // d.quant_tile) + 2 * d.d_rope) + 15) // 16 * 16
     q_idx_b = T * d.n_idx_heads * d.d_index + T * d.n_idx_heads * 4
     acct = {}
@@ -233,7 +233,7 @@ def accounting(wl, topk_host):
         bytes=len(sel_slots) * rec + q_b + out_b + 4 * T * d.top_k,
         logical_bytes=n_sel * rec + q_b + out_b + 4 * T * d.top_k,
         flops=2.0 * n_sel * d.n_heads * (2 * d.d_latent + d.d_rope), flop_dtype="bf16")
-    acct["kvpack_store"] = dict(bytes=T * (2 * d.d_latent + 2 * d.d_rope + d.d_index + 4 + 8) + T * (rec + idx_rec),
+    acct["kvpack_store"] = dict(bytes=T * (2 * d.d_latent + 2 * d.d_rope + d.key_bytes + 4 + 8) + T * (rec + idx_rec),
                                 flops=0.0, flop_dtype=None)
     acct["_step"] = dict(bytes=sum(v["bytes"] for v in acct.values()),
                          logical_bytes=sum(v.get("logical_bytes", v["bytes"]) for k, v in acct.items()),
@@ -283,9 +283,10 @@ def run_gpu(args):
     if world > 1:
         dist.barrier()
     smla.lib()
-    wl = make_config(args.workload, device="cuda", scale=args.scale)
+    wl = make_config(args.workload, device="cuda", scale=args.scale, key_format=args.key_format)
     d = wl.dims
-    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks,
+                           d.key_format)
     prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
     pool = torch.zeros(lay.pool_bytes, dtype=torch.uint8, device="cuda")
     s = wl.cached_slots
@@ -490,7 +491,7 @@ def run_gpu(args):
     step_b = acct["_step"]["bytes"]
     cpu = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(args.workload, budget_s=args.cpu_seconds)
+        cpu = cpu_baseline(args.workload, budget_s=args.cpu_seconds, key_format=args.key_format)
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_step, 4), "higher_is_better": True, "scaling": "weak",
@@ -532,14 +533,14 @@ class OracleSampler:
 
     max_rows = 4
 
-    def __init__(self, workload: int, max_seqs: int):
+    def __init__(self, workload: int, max_seqs: int, key_format: str = "e4m3"):
         from paged_sparse_mla_gb300.workloads import make_config
         import oracle
         self.oracle = oracle
-        self.wl = wl = make_config(workload, device="cpu")
+        self.wl = wl = make_config(workload, device="cpu", key_format=key_format)
         d = wl.dims
         self.lay = oracle.PoolLayout(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index,
-                                     wl.num_blocks)
+                                     wl.num_blocks, d.key_format)
         self.order = [int(b) for b in np.random.default_rng(7).permutation(wl.batch)[:max_seqs]]
         self.qsl = self._npy(wl.query_start_loc)
         self.next = 0
@@ -600,8 +601,8 @@ class OracleSampler:
         return done_tokens, spent, seqs
 
 
-def cpu_baseline(workload: int, budget_s: float):
-    sampler = OracleSampler(workload, max_seqs=64)
+def cpu_baseline(workload: int, budget_s: float, key_format: str = "e4m3"):
+    sampler = OracleSampler(workload, max_seqs=64, key_format=key_format)
     n, spent, seqs = sampler.run(budget_s)
     cores = len(os.sched_getaffinity(0))
     return {"value": round(n / spent, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
@@ -616,7 +617,7 @@ def run_reference(args):
         return
     # about two minutes of oracle work in all, split evenly over the warm-up and timed steps
     per_step = max(1.0, min(20.0, 120.0 / max(1, args.steps + args.warmup)))
-    sampler = OracleSampler(args.workload, max_seqs=8)
+    sampler = OracleSampler(args.workload, max_seqs=8, key_format=args.key_format)
     tok, spent_total, seqs_all = 0, 0.0, []
     for i in range(args.warmup + args.steps):
         n, spent, seqs = sampler.run(per_step)
@@ -659,11 +660,12 @@ def run_dcp(args):
     build_lib.build()
     smla.lib()
     n_sh = args.dcp
-    wl = make_config(args.workload, device="cuda", scale=args.scale)
+    wl = make_config(args.workload, device="cuda", scale=args.scale, key_format=args.key_format)
     if wl.max_q != 1:
         raise SystemExit("--dcp needs a decode workload with one query token per sequence (workloads 2 and 4)")
     d = wl.dims
-    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks,
+                           d.key_format)
     prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
     pool = torch.zeros(lay.pool_bytes, dtype=torch.uint8, device="cuda")
     s = wl.cached_slots
@@ -781,9 +783,10 @@ def run_hisparse(args):
     torch.cuda.set_device(0)
     build_lib.build()
     smla.lib()
-    wl = make_config(args.workload, device="cuda", scale=args.scale)
+    wl = make_config(args.workload, device="cuda", scale=args.scale, key_format=args.key_format)
     d = wl.dims
-    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    lay = smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks,
+                           d.key_format)
     prm = smla.make_params(d.n_heads, d.n_idx_heads, d.top_k, d.softmax_scale)
     pool = torch.zeros(lay.pool_bytes, dtype=torch.uint8, device="cuda")
     s = wl.cached_slots
@@ -942,6 +945,8 @@ def main():
                     help="split-context arm: N round-robin token shards on one GPU (decode workloads 2 and 4)")
     ap.add_argument("--scale", type=float, default=1.0,
                     help="shrink context lengths (profiler captures of a smaller case; not a bench line)")
+    ap.add_argument("--fp4-keys", dest="key_format", action="store_const", const="e2m1", default="e4m3",
+                    help="cache the indexer keys as packed FP4 E2M1 codes (workloads 2-5)")
     ap.add_argument("--topk-rows", action="store_true",
                     help="top-k arm: smla_topk alone on i.i.d. and on clustered score rows of the workload's shape")
     args = ap.parse_args()

@@ -75,12 +75,25 @@ typedef enum smla_status {
 } smla_status_t;
 
 /*
+ * Format of the cached indexer keys ([AgentX "Hybrid KV cache management"]:
+ * with the FP4 indexer the packed layout needs a smaller allocation unit).
+ *   SMLA_KEY_E4M3: d_index OCP FP8 E4M3 codes, one byte each.
+ *   SMLA_KEY_E2M1: d_index OCP MX FP4 E2M1 codes, two per byte (element 2i in
+ *                  the low nibble of byte i, element 2i+1 in the high nibble).
+ * Either way the key's fp32 scale s_I multiplies its score after the head sum.
+ */
+typedef enum smla_key_format {
+  SMLA_KEY_E4M3 = 0,
+  SMLA_KEY_E2M1 = 1
+} smla_key_format_t;
+
+/*
  * Packed block-pool layout ([AgentX "Hybrid KV cache management"]: all cache
  * groups and layers of a block in one contiguous allocation; the block is the
  * single allocation unit).  Per block, per layer l:
  *
  *   [block_size latent records, rec_stride bytes each]
- *   [block_size indexer keys, d_index e4m3 bytes each]
+ *   [block_size indexer keys, d_index (E4M3) or d_index/2 (E2M1) bytes each]
  *   [block_size indexer key scales, fp32]
  *
  * every region on a 256-byte boundary; a record is
@@ -101,7 +114,7 @@ typedef struct smla_layout {
   int32_t n_scales;       /* d_latent / quant_tile                             */
   int32_t rec_bytes;      /* d_latent + 4*n_scales + 2*d_rope                  */
   int32_t rec_stride;     /* rec_bytes rounded up to 16                        */
-  int32_t reserved0;
+  int32_t idx_key_format; /* smla_key_format_t of the cached indexer keys      */
   int64_t rec_off;        /* byte offset of the record region in a layer slice */
   int64_t idx_key_off;    /* byte offset of the indexer-key region             */
   int64_t idx_scale_off;  /* byte offset of the indexer-scale region           */
@@ -117,9 +130,19 @@ typedef struct smla_params {
   float softmax_scale;    /* sigma in s = sigma * (q.K + q_pe.kpe)             */
 } smla_params_t;
 
-/* Fill `layout` from the shape; checks divisibility.  Host only, no device work. */
+/* Fill `layout` from the shape, with E4M3 indexer keys; checks divisibility.
+ * Host only, no device work. */
 smla_status_t smla_layout_init(smla_layout_t* layout, int block_size, int n_layers, int d_latent,
                                int d_rope, int quant_tile, int d_index, int64_t num_blocks);
+
+/* smla_layout_init with the indexer-key format (an smla_key_format_t).  E2M1
+ * keys need d_index to be a multiple of 32; the key region then takes
+ * block_size * d_index / 2 bytes (for the DeepSeek shape the block of one layer
+ * shrinks from 50,432 to 46,336 bytes).  The indexer kernels are built for
+ * E2M1 keys with 64 indexer heads of 128 dims. */
+smla_status_t smla_layout_init_keys(smla_layout_t* layout, int block_size, int n_layers, int d_latent,
+                                    int d_rope, int quant_tile, int d_index, int key_format,
+                                    int64_t num_blocks);
 
 /* Bytes of `workspace` that smla_decode needs for these sizes (scores + top-k
  * scratch, then the split-attention scratch of smla_attend_workspace_size,
@@ -132,7 +155,8 @@ size_t smla_workspace_size(const smla_layout_t* layout, const smla_params_t* par
  * [GLM-5.3 "How to try", "Config and numbers"]: the KV cache is FP8.
  *   latent      bf16 [n_tokens, d_latent]
  *   rope        bf16 [n_tokens, d_rope]
- *   idx_k       e4m3 [n_tokens, d_index]   copied verbatim
+ *   idx_k       uint8 [n_tokens, key bytes] copied verbatim: d_index E4M3 codes,
+ *               or d_index/2 bytes of packed E2M1 codes (layout.idx_key_format)
  *   idx_scale   fp32 [n_tokens]            copied verbatim
  *   slot_mapping int64 [n_tokens]          physical slot (block*block_size+off); -1 = skip
  * Per quant_tile of the latent: scale = amax/448 (IEEE fp32 division; 1.0 if
@@ -149,8 +173,9 @@ smla_status_t kvpack_store(const smla_layout_t* layout, void* pool, int layer, c
  * [AgentX "DeepSeek V4"]: 64 indexer heads produce one global selection per
  * token; [GLM-5.3 "What is new"]: the indexer cost is quadratic in context.
  *   I[t, j] = s_I[j] * sum_h w[t, h] * ReLU(sum_d q_idx[t, h, d] * k_I[j, d]),  j <= p(t)
- * computed with FP8 tensor-core MMAs, fp32 accumulation and an fp32 head
- * reduction in head order.
+ * computed with FP8 tensor-core MMAs (E2M1 keys times E4M3 queries when the
+ * layout holds FP4 keys), fp32 accumulation and an fp32 head reduction in head
+ * order.
  *   q_idx   e4m3 [n_tokens, n_idx_heads, d_index]
  *   w       fp32 [n_tokens, n_idx_heads]
  *   scores  fp32 [n_tokens, scores_stride]: entries j <= p(t) are written,

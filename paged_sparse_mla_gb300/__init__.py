@@ -28,8 +28,10 @@ EXPORTED_SYMBOLS = (
     "smla_layout_init", "smla_workspace_size", "kvpack_store", "smla_index_scores", "smla_topk",
     "smla_attend", "smla_decode", "smla_get_last_error", "smla_status_string", "smla_version",
     "smla_decode_static", "smla_prefill_chunk", "smla_dcp_topk_merge", "smla_lse_merge", "smla_attend_hisparse",
-    "smla_selftest_wait", "smla_attend_workspace_size", "smla_topk_workspace_size",
+    "smla_selftest_wait", "smla_attend_workspace_size", "smla_topk_workspace_size", "smla_layout_init_keys",
 )
+
+KEY_FORMATS = {"e4m3": 0, "e2m1": 1}  # smla_key_format_t
 
 STATUS = {0: "SMLA_OK", 1: "SMLA_ERR_INVALID_ARG", 2: "SMLA_ERR_UNSUPPORTED", 3: "SMLA_ERR_CUDA",
           4: "SMLA_ERR_BAD_INDEX", 5: "SMLA_ERR_TIMEOUT", 6: "SMLA_ERR_SCRATCH_LIMIT"}
@@ -47,7 +49,7 @@ class Layout(ctypes.Structure):
         ("block_size", ctypes.c_int32), ("n_layers", ctypes.c_int32), ("d_latent", ctypes.c_int32),
         ("d_rope", ctypes.c_int32), ("quant_tile", ctypes.c_int32), ("d_index", ctypes.c_int32),
         ("num_blocks", ctypes.c_int64), ("n_scales", ctypes.c_int32), ("rec_bytes", ctypes.c_int32),
-        ("rec_stride", ctypes.c_int32), ("reserved0", ctypes.c_int32), ("rec_off", ctypes.c_int64),
+        ("rec_stride", ctypes.c_int32), ("idx_key_format", ctypes.c_int32), ("rec_off", ctypes.c_int64),
         ("idx_key_off", ctypes.c_int64), ("idx_scale_off", ctypes.c_int64), ("layer_stride", ctypes.c_int64),
         ("block_stride", ctypes.c_int64),
     ]
@@ -55,6 +57,11 @@ class Layout(ctypes.Structure):
     @property
     def pool_bytes(self) -> int:
         return self.num_blocks * self.block_stride
+
+    @property
+    def key_bytes(self) -> int:
+        """Bytes of one cached indexer key: d_index E4M3 codes, or d_index / 2 bytes of packed E2M1."""
+        return self.d_index // 2 if self.idx_key_format == KEY_FORMATS["e2m1"] else self.d_index
 
 
 class Params(ctypes.Structure):
@@ -79,6 +86,7 @@ def lib() -> ctypes.CDLL:
         LP, PP = ctypes.POINTER(Layout), ctypes.POINTER(Params)
         sig = {
             "smla_layout_init": (_I, [LP, _I, _I, _I, _I, _I, _I, _I64]),
+            "smla_layout_init_keys": (_I, [LP, _I, _I, _I, _I, _I, _I, _I, _I64]),
             "smla_workspace_size": (ctypes.c_size_t, [LP, PP, _I, _I]),
             "kvpack_store": (_I, [LP, _P, _I, _P, _P, _P, _P, _P, _I, _P]),
             "smla_index_scores": (_I, [LP, PP, _P, _I, _P, _P, _P, _I, _P, _P, _I, _I, _I, _I, _P, _I64, _P]),
@@ -175,7 +183,7 @@ def _need_new_tokens(layout, n, latent, rope, idx_k, idx_scale, slot_mapping, wh
     _need(slot_mapping, torch.int64, "slot_mapping", n)
     _need(latent, torch.bfloat16, f"{what}_latent", n * layout.d_latent)
     _need(rope, torch.bfloat16, f"{what}_rope", n * layout.d_rope)
-    _need(idx_k, torch.uint8, f"{what}_idx_k", n * layout.d_index)
+    _need(idx_k, torch.uint8, f"{what}_idx_k", n * layout.key_bytes)
     _need(idx_scale, torch.float32, f"{what}_idx_scale", n)
 
 
@@ -187,10 +195,17 @@ def status_string(code: int) -> str:
     return lib().smla_status_string(code).decode()
 
 
-def layout_init(block_size, n_layers, d_latent, d_rope, quant_tile, d_index, num_blocks) -> Layout:
+def layout_init(block_size, n_layers, d_latent, d_rope, quant_tile, d_index, num_blocks, key_format="e4m3") -> Layout:
+    """smla_layout_init (E4M3 indexer keys) or, with key_format="e2m1", smla_layout_init_keys (packed FP4 keys)."""
     lay = Layout()
-    _check(lib().smla_layout_init(ctypes.byref(lay), block_size, n_layers, d_latent, d_rope, quant_tile, d_index,
-                                  num_blocks), "smla_layout_init")
+    if key_format == "e4m3":
+        _check(lib().smla_layout_init(ctypes.byref(lay), block_size, n_layers, d_latent, d_rope, quant_tile, d_index,
+                                      num_blocks), "smla_layout_init")
+    else:
+        if key_format not in KEY_FORMATS:
+            raise ValueError(f"unknown indexer key format {key_format!r}")
+        _check(lib().smla_layout_init_keys(ctypes.byref(lay), block_size, n_layers, d_latent, d_rope, quant_tile,
+                                           d_index, KEY_FORMATS[key_format], num_blocks), "smla_layout_init_keys")
     return lay
 
 
@@ -208,7 +223,7 @@ def kvpack_store(layout, pool, layer, latent, rope, idx_k, idx_scale, slot_mappi
     _need(pool, torch.uint8, "pool", layout.pool_bytes)
     _need(latent, torch.bfloat16, "latent", n * layout.d_latent)
     _need(rope, torch.bfloat16, "rope", n * layout.d_rope)
-    _need(idx_k, torch.uint8, "idx_k", n * layout.d_index)
+    _need(idx_k, torch.uint8, "idx_k", n * layout.key_bytes)
     _need(idx_scale, torch.float32, "idx_scale", n)
     _check(lib().kvpack_store(ctypes.byref(layout), _ptr(pool), layer, _ptr(latent), _ptr(rope), _ptr(idx_k),
                               _ptr(idx_scale), _ptr(slot_mapping), n, _stream(stream)), "kvpack_store")

@@ -114,10 +114,10 @@ smla_status_t checked_device(unsigned** err) {
 bool layout_ok(const smla_layout_t* l) {
   if (l == nullptr) return false;
   smla_layout_t ref;
-  if (smla_layout_init(&ref, l->block_size, l->n_layers, l->d_latent, l->d_rope, l->quant_tile, l->d_index,
-                       l->num_blocks) != SMLA_OK)
+  if (smla_layout_init_keys(&ref, l->block_size, l->n_layers, l->d_latent, l->d_rope, l->quant_tile, l->d_index,
+                            l->idx_key_format, l->num_blocks) != SMLA_OK)
     return false;
-  return l->n_scales == ref.n_scales && l->rec_bytes == ref.rec_bytes && l->rec_stride == ref.rec_stride &&
+  return l->idx_key_format == ref.idx_key_format && l->n_scales == ref.n_scales && l->rec_bytes == ref.rec_bytes && l->rec_stride == ref.rec_stride &&
          l->rec_off == ref.rec_off && l->idx_key_off == ref.idx_key_off && l->idx_scale_off == ref.idx_scale_off &&
          l->layer_stride == ref.layer_stride && l->block_stride == ref.block_stride;
 }
@@ -167,10 +167,18 @@ const char* smla_status_string(smla_status_t s) {
 
 smla_status_t smla_layout_init(smla_layout_t* l, int block_size, int n_layers, int d_latent, int d_rope,
                                int quant_tile, int d_index, int64_t num_blocks) {
+  return smla_layout_init_keys(l, block_size, n_layers, d_latent, d_rope, quant_tile, d_index, SMLA_KEY_E4M3,
+                               num_blocks);
+}
+
+smla_status_t smla_layout_init_keys(smla_layout_t* l, int block_size, int n_layers, int d_latent, int d_rope,
+                                    int quant_tile, int d_index, int key_format, int64_t num_blocks) {
   if (l == nullptr || block_size <= 0 || n_layers <= 0 || d_latent <= 0 || d_rope < 0 || quant_tile <= 0 ||
       d_index <= 0 || num_blocks <= 0)
     return SMLA_ERR_INVALID_ARG;
   if (d_latent % quant_tile != 0 || d_latent % 32 != 0 || d_rope % 2 != 0 || d_index % 16 != 0)
+    return SMLA_ERR_INVALID_ARG;
+  if (key_format != SMLA_KEY_E4M3 && (key_format != SMLA_KEY_E2M1 || d_index % 32 != 0))
     return SMLA_ERR_INVALID_ARG;
   const int e = d_latent / 32;  // latent elements per lane in the store
   if (quant_tile % e != 0 || (quant_tile / e) > 32 || ((quant_tile / e) & (quant_tile / e - 1)) != 0)
@@ -182,13 +190,14 @@ smla_status_t smla_layout_init(smla_layout_t* l, int block_size, int n_layers, i
   l->d_rope = d_rope;
   l->quant_tile = quant_tile;
   l->d_index = d_index;
+  l->idx_key_format = key_format;
   l->num_blocks = num_blocks;
   l->n_scales = d_latent / quant_tile;
   l->rec_bytes = d_latent + 4 * l->n_scales + 2 * d_rope;
   l->rec_stride = static_cast<int32_t>(round_up(l->rec_bytes, 16));
   l->rec_off = 0;
   l->idx_key_off = round_up(static_cast<int64_t>(block_size) * l->rec_stride, 256);
-  l->idx_scale_off = round_up(l->idx_key_off + static_cast<int64_t>(block_size) * d_index, 256);
+  l->idx_scale_off = round_up(l->idx_key_off + static_cast<int64_t>(block_size) * key_bytes_of(d_index, key_format), 256);
   l->layer_stride = round_up(l->idx_scale_off + 4ll * block_size, 256);
   l->block_stride = l->layer_stride * n_layers;
   return SMLA_OK;

@@ -29,6 +29,15 @@
 //     bulk copy of its weights; completion is counted in transaction bytes on
 //     the stage's mbarrier;
 //   * warp 17 issues the MMAs and owns the tensor-memory allocation.
+//
+// FP4 keys ([AgentX "Hybrid KV cache management"]: the FP4 indexer shrinks the
+// packed block): the pool holds each key as 128 packed E2M1 codes (64 bytes).
+// The key copy uses the tensor map's 4-bit unpacking type, which places every
+// 16 codes (8 bytes) in a 16-byte shared-memory chunk followed by 8 bytes of
+// padding -- the layout tcgen05.mma.kind::f8f6f4 reads 4-bit operands in -- so
+// the key tile keeps the 128-byte rows and swizzle of the E4M3 tile, and the
+// MMA takes E2M1 keys (A) times E4M3 queries (B) at the FP8 rate while the key
+// stream from HBM is halved.
 #include "smla_internal.h"
 
 namespace smla {
@@ -49,6 +58,12 @@ constexpr int kEpiRegs = 104;
 constexpr int kOtherRegs = 56;
 static_assert(32 * kEpiWarps * kEpiRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr int kMaxN = 256;         // MMA N limit
+// Transaction bytes a 4-bit-unpacking key copy completes on its mbarrier: the bytes it writes to
+// shared memory (two per packed byte read).
+constexpr bool kUnpackTxIsSmemBytes = true;
+// Instruction-descriptor operand formats of kind::f8f6f4.
+constexpr int kFmtE4M3 = 0;
+constexpr int kFmtE2M1 = 5;
 constexpr int kMaxSeqSmem = 1024;  // batches up to this size are scheduled densely
 
 struct __align__(1024) IdxSmem {
@@ -225,7 +240,7 @@ __device__ __forceinline__ int mma_n(int n_grp, int heads) {
   return max(16, (n + 15) & ~15);
 }
 
-template <int kH, int kD, int kBS>
+template <int kH, int kD, int kBS, bool kFP4>
 __global__ void __launch_bounds__(kThreads, 1)
     index_scores_kernel(const IdxArgs A, const __grid_constant__ CUtensorMap key_map,
                         const __grid_constant__ CUtensorMap q_map) {
@@ -237,6 +252,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int kBlocks = kTile / kBS;  // blocks per tile
   static_assert(kTile % kBS == 0 && kBlocks <= 32 && kBS % 4 == 0, "tile geometry");
   static_assert(H % 4 == 0 && H * kGroup <= kMaxN, "head geometry");
+  static_assert(!kFP4 || kD == 128, "FP4 keys are built for 128-dim keys (128-byte unpacked rows)");
+  // shared-memory bytes of one key tile; with FP4 keys the copy reads half of them from global memory
+  constexpr uint32_t kKeyTileTx = (kFP4 && !kUnpackTxIsSmemBytes) ? kTile * kD / 2 : kTile * kD;
   const bool dense = A.batch <= kMaxSeqSmem;
 
   if (threadIdx.x == 0) {
@@ -339,7 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        if (lane == 0) mbar_arrive_expect_tx(&sm.key_full[s], kTile * kD + n_have * kBS * 4);
+        if (lane == 0) mbar_arrive_expect_tx(&sm.key_full[s], kKeyTileTx + n_have * kBS * 4);
         __syncwarp();
         if (lane < kBlocks) {
           tma_load_3d(smem_u32(sm.keys[s]) + lane * kBS * kD, &key_map, 0, 0, blk, &sm.key_full[s]);
@@ -378,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qb = nitem & 1;
         if (!mbar_wait(&sm.q_full[qb], (nitem >> 1) & 1, A.err, abort)) break;
         const int n = mma_n(it.n_grp, H);
-        const uint32_t idesc = make_idesc(128, n, 0, 0, 0, 0);
+        const uint32_t idesc = make_idesc(128, n, kFP4 ? kFmtE2M1 : kFmtE4M3, kFmtE4M3, 0, 0);
         const uint32_t qaddr = smem_u32(sm.q[qb]);
         bool ok = true;
         for (int tile = 0; tile < it.n_tiles; ++tile, ++k, ++a) {
@@ -496,22 +514,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ---------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ---------------------------------------------------------------------------
-template <int kH, int kD, int kBS>
+template <int kH, int kD, int kBS, bool kFP4>
 smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_rows, int grid, cudaStream_t stream) {
   EncodeTiledFn enc = encode_tiled();
   if (enc == nullptr) return SMLA_ERR_CUDA;
   const CUtensorMapSwizzle swz = kD == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_32B;
   CUtensorMap key_map, q_map;
   {
-    // keys: [num_blocks][block_size][kD] bytes of one layer's indexer-key region
+    // keys: [num_blocks][block_size][kD elements] of one layer's indexer-key region: kD bytes per key
+    // (E4M3), or kD / 2 bytes of packed E2M1 codes unpacked to 16-byte chunks by the copy
     void* base = const_cast<uint8_t*>(A.pool) + static_cast<int64_t>(A.layer) * A.L.layer_stride + A.L.idx_key_off;
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(kBS),
                                 static_cast<cuuint64_t>(A.L.num_blocks)};
-    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(A.L.block_stride)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(kFP4 ? kD / 2 : kD),
+                                   static_cast<cuuint64_t>(A.L.block_stride)};
     const cuuint32_t box[3] = {kD, kBS, 1};
     const cuuint32_t estr[3] = {1, 1, 1};
-    if (enc(&key_map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-            swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const CUtensorMapDataType kt = kFP4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    if (enc(&key_map, kt, 3, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
       return SMLA_ERR_CUDA;
   }
   {
@@ -530,17 +551,17 @@ smla_status_t launch_shape(const IdxArgs& A, const uint8_t* q_idx, int n_token_r
   const int dev = current_device_index();
   if (dev < 0) return SMLA_ERR_CUDA;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(index_scores_kernel<kH, kD, kBS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(index_scores_kernel<kH, kD, kBS, kFP4>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     // setmaxnreg.inc can only draw on the registers the CTA was launched with;
     // refuse to launch if the compiled allocation does not cover the split.
     cudaFuncAttributes fa;
-    if (cudaFuncGetAttributes(&fa, index_scores_kernel<kH, kD, kBS>) != cudaSuccess) return SMLA_ERR_CUDA;
+    if (cudaFuncGetAttributes(&fa, index_scores_kernel<kH, kD, kBS, kFP4>) != cudaSuccess) return SMLA_ERR_CUDA;
     if (fa.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set[dev].store(true, std::memory_order_release);
   }
-  index_scores_kernel<kH, kD, kBS><<<grid, kThreads, smem, stream>>>(A, key_map, q_map);
+  index_scores_kernel<kH, kD, kBS, kFP4><<<grid, kThreads, smem, stream>>>(A, key_map, q_map);
   return cudaGetLastError() == cudaSuccess ? SMLA_OK : SMLA_ERR_CUDA;
 }
 
@@ -561,10 +582,12 @@ EncodeTiledFn encode_tiled() {
   return fn;
 }
 
-// Shapes built into the library: (indexer heads, key dims, block size).
+// Shapes built into the library: (indexer heads, key dims, block size) with E4M3 keys; FP4 (E2M1)
+// keys with 64 heads of 128 dims.
 bool index_shape_supported(const KernelLayout& L, int n_idx_heads) {
-  return (n_idx_heads == 64 && L.d_index == 128 && (L.block_size == 64 || L.block_size == 16)) ||
-         (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16);
+  const bool deepseek = n_idx_heads == 64 && L.d_index == 128 && (L.block_size == 64 || L.block_size == 16);
+  if (L.key_format == SMLA_KEY_E2M1) return deepseek;
+  return L.key_format == SMLA_KEY_E4M3 && (deepseek || (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16));
 }
 
 smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const void* pool, int layer,
@@ -599,12 +622,15 @@ smla_status_t launch_index_scores(const KernelLayout& L, int n_idx_heads, const 
   const int grid = static_cast<int>(items < sms ? items : sms);
   // Query rows are addressed by absolute token (token t -> rows t*heads ..), so the map spans every
   // token below tok_end; the box of a group near the end reads past it as zeros.
+  const bool fp4 = L.key_format == SMLA_KEY_E2M1;
   if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 64)
-    return launch_shape<64, 128, 64>(A, q_idx, tok_end, grid, stream);
+    return fp4 ? launch_shape<64, 128, 64, true>(A, q_idx, tok_end, grid, stream)
+               : launch_shape<64, 128, 64, false>(A, q_idx, tok_end, grid, stream);
   if (n_idx_heads == 64 && L.d_index == 128 && L.block_size == 16)
-    return launch_shape<64, 128, 16>(A, q_idx, tok_end, grid, stream);
-  if (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16)
-    return launch_shape<4, 32, 16>(A, q_idx, tok_end, grid, stream);
+    return fp4 ? launch_shape<64, 128, 16, true>(A, q_idx, tok_end, grid, stream)
+               : launch_shape<64, 128, 16, false>(A, q_idx, tok_end, grid, stream);
+  if (n_idx_heads == 4 && L.d_index == 32 && L.block_size == 16 && !fp4)
+    return launch_shape<4, 32, 16, false>(A, q_idx, tok_end, grid, stream);
   return SMLA_ERR_UNSUPPORTED;
 }
 

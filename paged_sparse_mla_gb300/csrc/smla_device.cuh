@@ -306,7 +306,7 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t smem_addr, uint32_t lbo_
 }
 
 // Instruction descriptor: fp32 accumulate, M x N tile, operand formats and majors.
-//   fmt: kind::f16  -> 0 = F16, 1 = BF16;  kind::f8f6f4 -> 0 = E4M3, 1 = E5M2.
+//   fmt: kind::f16  -> 0 = F16, 1 = BF16;  kind::f8f6f4 -> 0 = E4M3, 1 = E5M2, 5 = E2M1.
 __host__ __device__ constexpr uint32_t make_idesc(int m, int n, int a_fmt, int b_fmt, int a_mn_major,
                                                   int b_mn_major) {
   return (1u << 4)                                   // D = F32

@@ -14,8 +14,14 @@ namespace smla {
 // Kernel-side copy of smla_layout_t (passed by value).
 struct KernelLayout {
   int32_t block_size, n_layers, d_latent, d_rope, quant_tile, d_index, n_scales, rec_stride;
+  int32_t key_format, key_bytes;  // smla_key_format_t; bytes of one cached indexer key
   int64_t num_blocks, rec_off, idx_key_off, idx_scale_off, layer_stride, block_stride;
 };
+
+// Bytes of one cached indexer key of d_index elements in the given format.
+inline int32_t key_bytes_of(int32_t d_index, int32_t key_format) {
+  return key_format == SMLA_KEY_E2M1 ? d_index / 2 : d_index;
+}
 
 inline KernelLayout kernel_layout(const smla_layout_t& l) {
   KernelLayout k;
@@ -27,6 +33,8 @@ inline KernelLayout kernel_layout(const smla_layout_t& l) {
   k.d_index = l.d_index;
   k.n_scales = l.n_scales;
   k.rec_stride = l.rec_stride;
+  k.key_format = l.idx_key_format;
+  k.key_bytes = key_bytes_of(l.d_index, l.idx_key_format);
   k.num_blocks = l.num_blocks;
   k.rec_off = l.rec_off;
   k.idx_key_off = l.idx_key_off;

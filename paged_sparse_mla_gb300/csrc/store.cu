@@ -62,9 +62,9 @@ __global__ void __launch_bounds__(256) kvpack_store_kernel(KernelLayout L, uint8
   uint16_t* rdst = reinterpret_cast<uint16_t*>(rec + L.d_latent + 4 * L.n_scales);
   for (int i = lane; i < L.d_rope; i += 32) rdst[i] = rsrc[i];
   // ---- indexer key (e4m3 bytes) and its fp32 scale verbatim ----
-  const uint8_t* ksrc = idx_k + static_cast<int64_t>(warp) * L.d_index;
-  uint8_t* kdst = layer_base + L.idx_key_off + static_cast<int64_t>(off) * L.d_index;
-  for (int i = lane; i < L.d_index; i += 32) kdst[i] = ksrc[i];
+  const uint8_t* ksrc = idx_k + static_cast<int64_t>(warp) * L.key_bytes;
+  uint8_t* kdst = layer_base + L.idx_key_off + static_cast<int64_t>(off) * L.key_bytes;
+  for (int i = lane; i < L.key_bytes; i += 32) kdst[i] = ksrc[i];
   if (lane == 0) {
     reinterpret_cast<float*>(layer_base + L.idx_scale_off)[off] = idx_scale[warp];
   }

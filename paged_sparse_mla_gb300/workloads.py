@@ -306,7 +306,7 @@ def shard_pools(wl: Workload, layout, pool: torch.Tensor, n_shards: int, *, seed
         lr = [shard_visible(int(n) - 1, r, n_shards) for n in lens]
         nblk = [(x + bs - 1) // bs for x in lr]
         total = sum(nblk) + 1
-        lay_r = layout_init(bs, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, total)
+        lay_r = layout_init(bs, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, total, d.key_format)
         pool_r = torch.zeros(lay_r.pool_bytes, dtype=torch.uint8, device=dev)
         perm = rng.permutation(total)
         bt_r = np.zeros((len(lens), max(1, max(nblk))), dtype=np.int32)
@@ -323,7 +323,7 @@ def shard_pools(wl: Workload, layout, pool: torch.Tensor, n_shards: int, *, seed
         dst_all = torch.as_tensor(np.concatenate(dst), device=dev)
         for c0 in range(0, src_all.numel(), 1 << 16):   # bounded index tensors
             src, dst = src_all[c0:c0 + (1 << 16)], dst_all[c0:c0 + (1 << 16)]
-            for name, unit in (("rec_off", layout.rec_stride), ("idx_key_off", layout.d_index), ("idx_scale_off", 4)):
+            for name, unit in (("rec_off", layout.rec_stride), ("idx_key_off", layout.key_bytes), ("idx_scale_off", 4)):
                 ar = torch.arange(unit, device=dev, dtype=torch.int64)
                 s0 = (src // bs) * layout.block_stride + layer * layout.layer_stride + getattr(layout, name) + \
                     (src % bs) * unit

@@ -75,6 +75,12 @@ int main(void) {
     }
   }
 
+  /* FP4 (E2M1) indexer keys: 64 packed bytes per key instead of 128 */
+  CHECK(40, smla_layout_init_keys(&lay, 64, 1, 512, 64, 128, 128, SMLA_KEY_E2M1, 1000) == SMLA_OK);
+  CHECK(41, lay.idx_key_format == SMLA_KEY_E2M1 && lay.idx_scale_off == 46080 && lay.block_stride == 46336);
+  CHECK(42, smla_layout_init_keys(&lay, 64, 1, 512, 64, 128, 128, 7, 1000) == SMLA_ERR_INVALID_ARG);
+  CHECK(43, smla_layout_init(&lay, 64, 1, 512, 64, 128, 128, 1000) == SMLA_OK && lay.idx_key_format == SMLA_KEY_E4M3);
+
   CHECK(12, strcmp(smla_status_string(SMLA_ERR_BAD_INDEX), "SMLA_ERR_BAD_INDEX") == 0);
   CHECK(13, strcmp(smla_status_string(SMLA_ERR_SCRATCH_LIMIT), "SMLA_ERR_SCRATCH_LIMIT") == 0);
   CHECK(14, smla_version() >= 100);

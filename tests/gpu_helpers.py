@@ -17,7 +17,8 @@ def ensure_built():
 
 def gpu_layout(wl):
     d = wl.dims
-    return smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks)
+    return smla.layout_init(d.block_size, d.n_layers, d.d_latent, d.d_rope, d.quant_tile, d.d_index, wl.num_blocks,
+                            d.key_format)
 
 
 def gpu_params(wl, top_k=None):

@@ -31,10 +31,12 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
-def test_layout_init_matches_oracle_layout(lib):
+@pytest.mark.parametrize("fmt", ["e4m3", "e2m1"])
+def test_layout_init_matches_oracle_layout(lib, fmt):
     for args in [(64, 1, 512, 64, 128, 128, 1000), (16, 1, 64, 16, 64, 32, 32), (64, 3, 512, 64, 128, 128, 7)]:
-        lay = smla.layout_init(*args)
-        ref = oracle.PoolLayout(*args)
+        lay = smla.layout_init(*args, key_format=fmt)
+        ref = oracle.PoolLayout(*args, fmt)
+        assert lay.key_bytes == ref.key_bytes and lay.idx_key_format == smla.KEY_FORMATS[fmt]
         assert lay.rec_stride == ref.rec_stride and lay.rec_bytes == ref.rec_bytes
         assert lay.idx_key_off == ref.idx_key_off and lay.idx_scale_off == ref.idx_scale_off
         assert lay.layer_stride == ref.layer_stride and lay.block_stride == ref.block_stride
@@ -48,6 +50,24 @@ def test_layout_init_rejects_bad_shapes(lib, bad):
     with pytest.raises(smla.SmlaError) as e:
         smla.layout_init(*bad)
     assert e.value.code == 1
+
+
+def test_fp4_key_layout_and_its_refusals(lib):
+    """smla_layout_init_keys: E2M1 keys halve the key region; unknown formats and d_index not a multiple
+    of 32 are refused; an E2M1 layout with a shape the FP4 indexer is not built for is UNSUPPORTED before
+    any device work."""
+    lay = smla.layout_init(64, 1, 512, 64, 128, 128, 10, key_format="e2m1")
+    assert (lay.idx_key_off, lay.idx_scale_off, lay.block_stride) == (41984, 46080, 46336)
+    L = ctypes.byref(smla.Layout())
+    assert lib.smla_layout_init_keys(L, 64, 1, 512, 64, 128, 128, 2, 10) == 1      # unknown format
+    assert lib.smla_layout_init_keys(L, 64, 1, 512, 64, 128, 48, 1, 10) == 1       # d_index % 32 != 0
+    assert lib.smla_layout_init_keys(L, 64, 1, 512, 64, 128, 48, 0, 10) == 0       # fine as E4M3
+    tiny = smla.layout_init(16, 1, 64, 16, 64, 32, 32, key_format="e2m1")
+    prm = smla.make_params(8, 4, 64, 0.1)
+    p = ctypes.c_void_p(4096)
+    step = (p, 0, p, p, p, p, p, p, p, p, p, p, 16, p, p, 1, 1, 1, 100, p, p, None)
+    assert lib.smla_decode(ctypes.byref(tiny), ctypes.byref(prm), *step, p, 1 << 30, None) == 2
+    assert lib.smla_decode_static(ctypes.byref(tiny), ctypes.byref(prm), *step, None) == 2
 
 
 def test_host_side_argument_checks(lib):
@@ -84,7 +104,8 @@ def test_host_side_argument_checks(lib):
 
 
 @pytest.mark.parametrize("field,delta", [("idx_key_off", 16), ("block_stride", -256), ("rec_stride", 16),
-                                         ("quant_tile", -128), ("layer_stride", 256), ("n_scales", 1)])
+                                         ("quant_tile", -128), ("layer_stride", 256), ("n_scales", 1),
+                                         ("idx_key_format", 1)])
 def test_layouts_not_made_by_layout_init_are_refused_everywhere(lib, field, delta):
     """Every entry point that takes a layout refuses one whose fields differ from smla_layout_init's,
     before any device work; the two fused entry points answer alike."""
