@@ -33,8 +33,9 @@
 // FP4 keys ([AgentX "Hybrid KV cache management"]: the FP4 indexer shrinks the
 // packed block): the pool holds each key as 128 packed E2M1 codes (64 bytes).
 // The key copy uses the tensor map's 4-bit unpacking type, which places every
-// 16 codes (8 bytes) in a 16-byte shared-memory chunk followed by 8 bytes of
-// padding -- the layout tcgen05.mma.kind::f8f6f4 reads 4-bit operands in -- so
+// 16 codes (8 bytes) at the start of a 16-byte shared-memory chunk, the other
+// 8 bytes being padding -- the layout tcgen05.mma.kind::f8f6f4 reads 4-bit
+// operands in -- so
 // the key tile keeps the 128-byte rows and swizzle of the E4M3 tile, and the
 // MMA takes E2M1 keys (A) times E4M3 queries (B) at the FP8 rate while the key
 // stream from HBM is halved.
@@ -58,9 +59,10 @@ constexpr int kEpiRegs = 104;
 constexpr int kOtherRegs = 56;
 static_assert(32 * kEpiWarps * kEpiRegs + 128 * kOtherRegs <= kThreads * kLaunchRegs, "register split exceeds the launch");
 constexpr int kMaxN = 256;         // MMA N limit
-// Transaction bytes a 4-bit-unpacking key copy completes on its mbarrier: the bytes it writes to
-// shared memory (two per packed byte read).
-constexpr bool kUnpackTxIsSmemBytes = true;
+// Transaction bytes a 4-bit-unpacking key copy completes on its mbarrier: the packed bytes it
+// reads from global memory (half of the shared-memory bytes it fills; measured on GB300).  The
+// padding half of each 16-byte chunk is left as it was; the MMA does not read it.
+constexpr bool kUnpackTxIsSmemBytes = false;
 // Instruction-descriptor operand formats of kind::f8f6f4.
 constexpr int kFmtE4M3 = 0;
 constexpr int kFmtE2M1 = 5;

@@ -7,9 +7,13 @@ exact radix select over the whole row when:
 
   overflow   one warp's list overflows: the top scores cluster in one segment
              (a contiguous run of high scores, the top k in the last 1/16 of the
-             row, a monotone row);
+             row, a monotone row); the hits are then collected once more into
+             lists packed one after another, or, beyond the buffer, the row
+             takes the radix select;
   miss       the sample overestimates the threshold and fewer than k positions
              reach it: the highest scores sit exactly at the sampled positions;
+  plateau    more positions reach the threshold than the candidate buffer holds
+             (8,192): a plateau of equal top scores;
   large k    k is above the fast path's limit (4,096);
   unaligned  the row does not start on a 16-byte boundary (an odd row stride).
 
@@ -115,6 +119,23 @@ def test_sample_misses_the_threshold(ties):
     rng = np.random.default_rng(202 + ties)
     rows = [sample_aligned_row(rng, m, ties) for m in (50, 64, 97)]
     _check(rows, _run_topk(rows, 2048), 2048, "sample miss")
+
+
+def test_plateau_of_ties_beyond_the_candidate_buffer():
+    rng = np.random.default_rng(207)
+    n = 120_000
+    rows = []
+    a = _background(rng, n)
+    a[rng.choice(n, 10_000, replace=False)] = np.float32(50.0)         # spread plateau
+    rows.append(a)
+    b = _background(rng, n)
+    b[30_000:42_000] = np.float32(50.0)                                # contiguous plateau
+    rows.append(b)
+    c = _background(rng, n)
+    c[rng.choice(n, 9_000, replace=False)] = np.float32(50.0)          # plateau with 1,000 above it
+    c[rng.choice(n, 1_000, replace=False)] = np.float32(60.0) + rng.integers(0, 5, 1_000).astype(np.float32)
+    rows.append(c)
+    _check(rows, _run_topk(rows, 2048), 2048, "plateau")
 
 
 def test_k_above_the_fast_path_limit():
