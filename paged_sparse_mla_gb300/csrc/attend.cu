@@ -421,7 +421,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Whole-record gather: producer warp pw takes keys pw, pw + 11, ...; for each key,
           // lane l loads latent piece l (16 codes) and, for l < 9, the piece after the latent
           // codes (lane 0: the four scales; lanes 1-8: the rope), so every record is read by
-          // two coalesced warp loads.  Two keys per batch, three batches per tile.
+          // two coalesced warp loads.  Two keys per batch, three batches per tile, two batches in
+          // registers: both are requested before the wait for the tile buffer (their latency
+          // overlaps the previous tiles' MMAs and softmax instead of following the buffer's
+          // release), and a batch register set is refilled with the third batch as soon as it has
+          // been stored.
           const int pw = warp - kFirstProducerWarp;
           constexpr int kPW = kProducerThreads / 32;
           constexpr int kR = 2;
@@ -463,12 +467,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           };
           constexpr int kNB = ((kTile + kPW - 1) / kPW + kR - 1) / kR;  // batches per tile
           load_batch(0, lat[0], ext[0]);
+          if (kNB > 1) load_batch(kR, lat[1], ext[1]);
           ok = mbar_wait(&sm.kv_empty[kb], ((kk >> 1) & 1) ^ 1, A.err, abort);
 #pragma unroll
           for (int bi = 0; bi < kNB; ++bi) {
-            if (bi + 1 < kNB) load_batch((bi + 1) * kR, lat[(bi + 1) & 1], ext[(bi + 1) & 1]);
             if (bi == 0) blk_ahead = block_of(j_ahead);
             store_batch(bi * kR, lat[bi & 1], ext[bi & 1]);
+            if (bi + 2 < kNB) load_batch((bi + 2) * kR, lat[bi & 1], ext[bi & 1]);
           }
         } else {
         // first batch of loads is issued before waiting for the tile buffer
@@ -687,30 +692,43 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sm.s_empty[kb]);  // the scores are in registers
-        // per-head maximum of this tile over the warp's keys; lane h keeps head 32 hh + h
-        {
-          float mine = -INFINITY;
+        // Does any running max have to move?  A head's max moves only when a score of this tile
+        // exceeds it by the threshold, so each thread first tests its own scores against the
+        // running maxima; the per-head tile maxima (a reduction across lanes and warps) are only
+        // formed when some thread found one, which after the first tile is rare.  A failed wait in
+        // any warp (here or in the previous tile's rescale) also takes that branch and ends the
+        // token for all warps at its barrier.
+        int exceed = tile == 0 || !ok;
+        if (!exceed) {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) {
-            const float m = warp_max(sc[h]);
-            mine = lane == h ? m : mine;
+          for (int h = 0; h < 32; ++h) exceed |= sc[h] > sm.m_run[32 * hh + h] + kRescaleThreshold;
+        }
+        bool moved = false;
+        if (bar_red_or(1, kSoftmaxThreads, exceed)) {
+          // per-head maximum of this tile over the warp's keys; lane h keeps head 32 hh + h
+          {
+            float mine = -INFINITY;
+#pragma unroll
+            for (int h = 0; h < 32; ++h) {
+              const float m = warp_max(sc[h]);
+              mine = lane == h ? m : mine;
+            }
+            sm.red[sp][32 * hh + lane] = mine;
           }
-          sm.red[sp][32 * hh + lane] = mine;
+          // this tile's maxima are complete
+          if (bar_red_or(1, kSoftmaxThreads, !ok)) {
+            failed = true;
+            break;
+          }
+          int need_h = 0;
+          if (tid < kHeads) {
+            const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
+            sm.m_tile[tid] = mt;
+            need_h = tile == 0 || mt > sm.m_run[tid] + kRescaleThreshold;
+          }
+          // one barrier that also ORs the per-head "running max must move" flags
+          moved = bar_red_or(1, kSoftmaxThreads, need_h) != 0;
         }
-        // this tile's maxima are complete; a failed wait in any warp (here or in the
-        // previous tile's rescale) ends the token for all of them
-        if (bar_red_or(1, kSoftmaxThreads, !ok)) {
-          failed = true;
-          break;
-        }
-        int need_h = 0;
-        if (tid < kHeads) {
-          const float mt = fmaxf(fmaxf(sm.red[0][tid], sm.red[1][tid]), fmaxf(sm.red[2][tid], sm.red[3][tid]));
-          sm.m_tile[tid] = mt;
-          need_h = tile == 0 || mt > sm.m_run[tid] + kRescaleThreshold;
-        }
-        // one barrier that also ORs the per-head "running max must move" flags
-        const bool moved = bar_red_or(1, kSoftmaxThreads, need_h) != 0;
         if (moved) {
           if (tid < kHeads) {
             const float old = tile == 0 ? -INFINITY : sm.m_run[tid];

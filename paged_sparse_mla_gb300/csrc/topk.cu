@@ -18,7 +18,10 @@
 //      before use and read again, +64 MB per launch and slower.)
 // If at least k were collected and no list overflowed, a radix select over the
 // lists gives the exact k-th largest key; keys above it are kept and ties keep
-// their lowest positions.  Because the lists are position-ordered and the
+// their lowest positions.  If some list overflowed but all the hits fit the
+// buffer (they cluster in a few warps' segments, as the highest scores of a real
+// row cluster on recent positions), the row is collected once more with every
+// warp's hits packed after those of the warps before it, and selected from there.  Because the lists are position-ordered and the
 // segments increase with the warp index, every warp writes its kept positions
 // straight to their output slots from per-warp prefix counts: the output is in
 // ascending order without a sort.  Rows with at most `capacity` positions take
@@ -45,6 +48,7 @@ struct TopkSmem {
   int warp_tot[32];
   int sel_bin, sel_above;
   int wcnt[kWarps], wgt[kWarps], weq[kWarps];  // per-warp candidate lists: length, > T, == T
+  int woff[kWarps];                             // packed lists (select_packed): start of each in cand
   // where the row's selection goes besides the output row (see RowOut), kept here rather than in
   // registers, which the collection pass needs
   int pos_base;
@@ -181,6 +185,7 @@ __device__ uint32_t radix_select(TopkSmem& sm, const uint32_t* keys, int n, int 
 // The k-th largest key among the per-warp candidate lists (warp w's list is
 // cand[w * kWarpCap .. + wcnt[w])).
 // `mask_out` gives the key bits the result decides: compare (key & mask_out) with it.
+template <bool kPacked>
 __device__ uint32_t radix_select_lists(TopkSmem& sm, int k, int& rem, uint32_t& mask_out) {
   uint32_t prefix = 0, mask = 0;
   int remaining = k;
@@ -195,7 +200,7 @@ __device__ uint32_t radix_select_lists(TopkSmem& sm, int k, int& rem, uint32_t& 
     {  // each warp histograms its own list
       const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
       const int cnt = sm.wcnt[warp];
-      const unsigned long long* list = sm.cand + warp * kWarpCap;
+      const unsigned long long* list = sm.cand + (kPacked ? sm.woff[warp] : warp * kWarpCap);
       for (int j0 = 0; j0 < cnt; j0 += 32) {
         const int j = j0 + lane;
         const bool in = j < cnt;
@@ -290,6 +295,124 @@ __device__ __forceinline__ int visible(const int32_t* seq_lens, const int32_t* q
   const int b = seq_of_token(qsl, batch, t);
   const int q0 = __ldg(qsl + b), n_q = __ldg(qsl + b + 1) - q0;
   return __ldg(seq_lens + b) - n_q + (t - q0) + 1;
+}
+
+// The exact top-k among the per-warp candidate lists (list w: `list_off` entries into cand for the
+// calling warp, wcnt[w] long; kPacked: the lists sit at woff[w]), written in position order.
+template <bool kPlain, bool kPacked>
+__device__ __forceinline__ void select_from_lists(TopkSmem& sm, const float* __restrict__ s, int k, int32_t* o,
+                                                  int list_off, int count) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned long long* list = sm.cand + list_off;
+  // ---- exact k-th largest key T among the candidates ----
+  int need_eq;
+  uint32_t tmask;
+  const uint32_t T = radix_select_lists<kPacked>(sm, k, need_eq, tmask);
+  // ---- every warp counts its keys above T and equal to T ----
+  {
+    int gt = 0, eq = 0;
+    for (int j = lane; j < count; j += 32) {
+      const uint32_t key = static_cast<uint32_t>(list[j] >> 32) & tmask;
+      gt += key > T;
+      eq += key == T;
+    }
+#pragma unroll
+    for (int o2 = 16; o2 > 0; o2 >>= 1) {
+      gt += __shfl_xor_sync(0xffffffffu, gt, o2);
+      eq += __shfl_xor_sync(0xffffffffu, eq, o2);
+    }
+    if (lane == 0) {
+      sm.wgt[warp] = gt;
+      sm.weq[warp] = eq;
+    }
+  }
+  __syncthreads();
+  // ---- lists are in position order and warps cover increasing segments: each warp writes its
+  // kept positions straight to their output slots (ties keep the lowest positions) ----
+  int eq_before = 0, out_off = 0;
+  for (int w = 0; w < warp; ++w) {
+    const int take = max(0, min(sm.weq[w], need_eq - eq_before));
+    eq_before += sm.weq[w];
+    out_off += sm.wgt[w] + take;
+  }
+  const int take_eq = max(0, min(sm.weq[warp], need_eq - eq_before));
+  int written = 0, ties_seen = 0;
+  for (int j0 = 0; j0 < count; j0 += 32) {
+    const int j = j0 + lane;
+    uint32_t key = 0;
+    int pos = 0;
+    if (j < count) {
+      key = static_cast<uint32_t>(list[j] >> 32) & tmask;
+      pos = static_cast<int>(~static_cast<uint32_t>(list[j] & 0xFFFFFFFFull));
+    }
+    const bool is_eq = j < count && key == T;
+    const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
+    const uint32_t below = (1u << lane) - 1u;
+    const bool keep = j < count && (key > T || (is_eq && ties_seen + __popc(eq_mask & below) < take_eq));
+    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
+    if (keep) emit<kPlain>(sm, o, s, out_off + written + __popc(keep_mask & below), pos);
+    written += __popc(keep_mask);
+    ties_seen += __popc(eq_mask);
+  }
+}
+
+// Rows whose hits overflow some warp's list but fit the buffer together: the hits cluster in a few
+// warps' segments (as the highest scores of a real row cluster on recent positions).  Each warp
+// collects its hits again (same row, same threshold) after those of the warps before it, so the
+// lists stay in position order, and the selection runs over the packed lists.
+template <bool kPlain>
+__device__ void select_packed(TopkSmem& sm, const float* __restrict__ s, int k, int32_t* o, int p_lo,
+                                           int p_hi, uint32_t thr) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += sm.wcnt[w];
+  __syncthreads();  // every warp has read the counts before any list is overwritten
+  unsigned long long* list = sm.cand + before;
+  const int cap = kCap - before;
+  int count = 0;
+  for (int base = p_lo; base < p_hi; base += kSpan) {
+    const int p0 = base + 16 * lane;
+    uint32_t hit = 0;
+    uint32_t keys[16];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
+      const int j = p0 + 4 * u;
+      if (j + 3 < p_hi) {
+        v = __ldg(reinterpret_cast<const float4*>(s + j));
+      } else {
+        if (j < p_hi) v.x = __ldg(s + j);
+        if (j + 1 < p_hi) v.y = __ldg(s + j + 1);
+        if (j + 2 < p_hi) v.z = __ldg(s + j + 2);
+      }
+      keys[4 * u] = order_key(v.x);
+      keys[4 * u + 1] = order_key(v.y);
+      keys[4 * u + 2] = order_key(v.z);
+      keys[4 * u + 3] = order_key(v.w);
+    }
+#pragma unroll
+    for (int e = 0; e < 16; ++e)
+      if (p0 + e < p_hi && keys[e] >= thr) hit |= 1u << e;
+    const int cnt = __popc(hit);
+    int incl = cnt;
+#pragma unroll
+    for (int o2 = 1; o2 < 32; o2 <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o2);
+      if (lane >= o2) incl += y;
+    }
+    int pos = count + incl - cnt;
+    while (hit) {
+      const int e = __ffs(hit) - 1;
+      hit &= hit - 1;
+      if (pos < cap)
+        list[pos] = (static_cast<unsigned long long>(keys[e]) << 32) | static_cast<uint32_t>(~(p0 + e));
+      ++pos;
+    }
+    count += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  if (lane == 0) sm.woff[warp] = before;
+  __syncthreads();
+  select_from_lists<kPlain, true>(sm, s, k, o, before, sm.wcnt[warp]);
 }
 
 // The top-k of the n scores s[0..n) (every thread of the CTA; each branch below is CTA-uniform).
@@ -407,60 +530,15 @@ __device__ void topk_core(TopkSmem& sm, const float* __restrict__ s, int n, int 
     n_cand += sm.wcnt[w];
     over |= sm.wcnt[w] > kWarpCap;
   }
+  if (over && n_cand >= k && n_cand <= kCap) {  // clustered hits: collect them again, packed
+    select_packed<kPlain>(sm, s, k, o, p_lo, p_hi, thr);
+    return;
+  }
   if (n_cand < k || over) {  // the sample's guess missed: exact radix select over the row
     topk_slow<kPlain>(sm, s, n, k, o);
     return;
   }
-  // ---- exact k-th largest key T among the candidates ----
-  int need_eq;
-  uint32_t tmask;
-  const uint32_t T = radix_select_lists(sm, k, need_eq, tmask);
-  // ---- every warp counts its keys above T and equal to T ----
-  {
-    int gt = 0, eq = 0;
-    for (int j = lane; j < count; j += 32) {
-      const uint32_t key = static_cast<uint32_t>(list[j] >> 32) & tmask;
-      gt += key > T;
-      eq += key == T;
-    }
-#pragma unroll
-    for (int o2 = 16; o2 > 0; o2 >>= 1) {
-      gt += __shfl_xor_sync(0xffffffffu, gt, o2);
-      eq += __shfl_xor_sync(0xffffffffu, eq, o2);
-    }
-    if (lane == 0) {
-      sm.wgt[warp] = gt;
-      sm.weq[warp] = eq;
-    }
-  }
-  __syncthreads();
-  // ---- lists are in position order and warps cover increasing segments: each warp writes its
-  // kept positions straight to their output slots (ties keep the lowest positions) ----
-  int eq_before = 0, out_off = 0;
-  for (int w = 0; w < warp; ++w) {
-    const int take = max(0, min(sm.weq[w], need_eq - eq_before));
-    eq_before += sm.weq[w];
-    out_off += sm.wgt[w] + take;
-  }
-  const int take_eq = max(0, min(sm.weq[warp], need_eq - eq_before));
-  int written = 0, ties_seen = 0;
-  for (int j0 = 0; j0 < count; j0 += 32) {
-    const int j = j0 + lane;
-    uint32_t key = 0;
-    int pos = 0;
-    if (j < count) {
-      key = static_cast<uint32_t>(list[j] >> 32) & tmask;
-      pos = static_cast<int>(~static_cast<uint32_t>(list[j] & 0xFFFFFFFFull));
-    }
-    const bool is_eq = j < count && key == T;
-    const uint32_t eq_mask = __ballot_sync(0xffffffffu, is_eq);
-    const uint32_t below = (1u << lane) - 1u;
-    const bool keep = j < count && (key > T || (is_eq && ties_seen + __popc(eq_mask & below) < take_eq));
-    const uint32_t keep_mask = __ballot_sync(0xffffffffu, keep);
-    if (keep) emit<kPlain>(sm, o, s, out_off + written + __popc(keep_mask & below), pos);
-    written += __popc(keep_mask);
-    ties_seen += __popc(eq_mask);
-  }
+  select_from_lists<kPlain, false>(sm, s, k, o, warp * kWarpCap, count);
 }
 
 // One CTA per row while the rows fit one wave of resident CTAs.  Beyond that the grid is
