@@ -548,21 +548,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dv21 = sw128_desc(smem_u32(sm.kv[1][0]), kChunkBytes, 1024);
       const uint64_t dp20 = sw128_desc(smem_u32(sm.kv[0][kLatChunks]), kChunkBytes, 1024);
       const uint64_t dp21 = sw128_desc(smem_u32(sm.kv[1][kLatChunks]), kChunkBytes, 1024);
-      // MMA1 of global tile k1: S^T = Khat . q^T over 576 dims into S buffer k1 % 2.
-      const auto mma1 = [&](uint32_t k1) {
-        const int b1 = k1 & 1;
-        const uint64_t ka = b1 ? dk11 : dk10;
-        const uint32_t ts = tmem_s + b1 * kHeads;
-#pragma unroll
-        for (int c = 0; c < NCH; ++c) {
-#pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            mma_f16(ts, ka + ((c * kChunkBytes + k4 * 32) >> 4), dq + ((c * kHeads * 128 + k4 * 32) >> 4), idesc1,
-                    (c | k4) != 0);
-          }
-        }
-        mma_commit(&sm.s_full[b1]);
-      };
       // MMA2 of global tile k2: O^T += V^T . P^T over the tile's 64 keys.
       const auto mma2 = [&](uint32_t k2, bool first) {
         const int b2 = k2 & 1;
@@ -576,6 +561,26 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         mma_commit(&sm.kv_empty[b2]);
+      };
+      // MMA1 of global tile k1: S^T = Khat . q^T over 576 dims into S buffer k1 % 2.  Every three
+      // 64-dim chunks it calls between(): the previous tile's MMA2 is issued there as soon as its
+      // probabilities are written, instead of after all 36 MMA1 instructions, so that tile's
+      // buffer goes back to the producers sooner.  (The tensor pipe runs the instructions in
+      // issue order; each commit covers everything issued before it.)
+      const auto mma1 = [&](uint32_t k1, auto&& between) {
+        const int b1 = k1 & 1;
+        const uint64_t ka = b1 ? dk11 : dk10;
+        const uint32_t ts = tmem_s + b1 * kHeads;
+#pragma unroll
+        for (int c = 0; c < NCH; ++c) {
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            mma_f16(ts, ka + ((c * kChunkBytes + k4 * 32) >> 4), dq + ((c * kHeads * 128 + k4 * 32) >> 4), idesc1,
+                    (c | k4) != 0);
+          }
+          if (c % 3 == 2 && c + 1 < NCH) between();
+        }
+        mma_commit(&sm.s_full[b1]);
       };
       const int n_units = A.n_rows * (SPLIT ? A.n_splits : 1);
       for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++n) {
@@ -591,6 +596,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t k1 = kbeg, k2 = kbeg;
         uint64_t t_last = globaltimer_ns();
         bool ok = true;
+        // during MMA1 of tile k1 the only MMA2 that can be pending is tile k1 - 1's
+        const auto mma2_if_ready = [&]() {
+          if (k2 < k1 && mbar_test(&sm.p_full[k2 & 1], (k2 >> 1) & 1)) {
+            tc_fence_after();
+            mma2(k2, k2 == kbeg);
+            ++k2;
+          }
+        };
         while (k2 < kend) {
           bool progress = false;
           if (k2 < k1 && mbar_test(&sm.p_full[k2 & 1], (k2 >> 1) & 1)) {
@@ -601,7 +614,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else if (k1 < kend && mbar_test(&sm.kv_full[k1 & 1], (k1 >> 1) & 1) &&
                      mbar_test(&sm.s_empty[k1 & 1], ((k1 >> 1) & 1) ^ 1)) {
             tc_fence_after();
-            mma1(k1);
+            mma1(k1, mma2_if_ready);
             issued = true;
             if (k1 == kend - 1) mma_commit(&sm.q_empty);
             ++k1;
