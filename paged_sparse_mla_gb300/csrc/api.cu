@@ -217,8 +217,10 @@ size_t smla_workspace_size(const smla_layout_t* layout, const smla_params_t* par
 
 size_t smla_attend_workspace_size(const smla_layout_t* layout, const smla_params_t* params, int n_tokens) {
   if (!layout_ok(layout) || params == nullptr || n_tokens <= 0 || params->n_heads <= 0) return 0;
-  // rows fewer than the SMs are split; rows x splits stay within kMaxSplitUnits (>= any SM count)
-  return n_tokens < kMaxSplitUnits ? attend_split_bytes(params->n_heads, layout->d_latent, kMaxSplitUnits) : 0;
+  // rows fewer than the SMs are split (rows x splits stay within kMaxSplitUnits, >= any SM count);
+  // up to eight rows per SM are balanced over the SMs (two partial slots per SM)
+  return n_tokens < 8 * kMaxSplitUnits ? attend_split_bytes(params->n_heads, layout->d_latent, 2 * kMaxSplitUnits)
+                                       : 0;
 }
 
 smla_status_t kvpack_store(const smla_layout_t* layout, void* pool, int layer, const void* latent, const void* rope,

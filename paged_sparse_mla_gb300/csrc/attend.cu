@@ -107,7 +107,44 @@ struct AttnArgs {
   int n_splits;
   float* part_out;
   float* part_lse;
+  // Balanced units (mode 2): CTA c takes the nominal tiles [c * T / G, (c + 1) * T / G) of the
+  // n_rows * row_tiles_nom tiles, G = gridDim.x.  A row is then split over at most two CTAs: the
+  // first CTA's part goes to partial slot 2c + 1, the second's to slot 2 (c + 1); whole rows are
+  // written directly.
+  int row_tiles_nom;
+  int mode;  // 0 plain, 1 split, 2 balanced
 };
+
+// Work units of a CTA: kMode 0, rows c, c + G, ...; kMode 1, (row, split) pairs u = c, c + G, ...
+// with u = row * n_splits + split (the split's tile range follows from the row's valid tiles);
+// kMode 2, the rows its balanced range of nominal tiles meets, with tiles [ta, tb) of each.
+// slot: the partial-output slot of the unit, or -1 when it writes the row's output itself.
+template <int kMode>
+__device__ __forceinline__ bool unit_at(const AttnArgs& A, int i, int& tr, int& split, int& ta, int& tb, int& slot) {
+  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
+  if constexpr (kMode == 2) {
+    const int64_t T = A.row_tiles_nom, tot = static_cast<int64_t>(A.n_rows) * T;
+    const int64_t g0 = c * tot / G, g1 = (c + 1) * tot / G;
+    const int64_t r = g0 / T + i;
+    if (r * T >= g1) return false;
+    tr = static_cast<int>(r);
+    split = 0;
+    ta = static_cast<int>(max(g0, r * T) - r * T);
+    tb = static_cast<int>(min(g1, (r + 1) * T) - r * T);
+    slot = (ta == 0 && tb == T) ? -1 : (ta > 0 ? 2 * c : 2 * c + 1);
+    return true;
+  } else {
+    const int n_splits = kMode == 1 ? A.n_splits : 1;
+    const int u = c + i * G;
+    if (u >= A.n_rows * n_splits) return false;
+    tr = u / n_splits;
+    split = u % n_splits;
+    ta = 0;
+    tb = 0x7fffffff;
+    slot = kMode == 1 ? split * A.n_rows + tr : -1;
+    return true;
+  }
+}
 
 // Transpose-reduce 32 per-lane values across the 32 lanes of a warp: afterwards
 // lane l holds the reduction of value l in v[0].
@@ -258,7 +295,7 @@ __device__ __forceinline__ int row_tiles(const int32_t* row, int k, int lane) {
   return (last + kTile) / kTile;
 }
 
-template <int NCH, bool WR, bool SPLIT>
+template <int NCH, bool WR, int MODE>
 __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const AttnArgs A, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap qpe_map) {
@@ -314,20 +351,20 @@ __global__ void __launch_bounds__(kThreads, 1)
     // group barrier (what it writes meanwhile is discarded), where the failure is ORed in
     // (bar.red), so that every producer warp leaves the loop together and none is left
     // waiting at a named barrier.
-    const int n_splits = SPLIT ? A.n_splits : 1;  // compile-time 1 without the split
-    const int n_units = A.n_rows * n_splits;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
-      const int tr = u / n_splits, split = u % n_splits;
+    const int n_splits = MODE == 1 ? A.n_splits : 1;  // compile-time 1 without the split
+    int tr, split, ta, tb_nom, slot;
+    for (int ui = 0; unit_at<MODE>(A, ui, tr, split, ta, tb_nom, slot); ++ui, ++n) {
       const int t = A.tok_begin + tr;
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
       const int row_nt = row_tiles(idx, A.top_k, lane);
-      const int tb = split * row_nt / n_splits;  // this unit's tiles: [tb, tb + ntiles) of the row
-      const int ntiles = (split + 1) * row_nt / n_splits - tb;
+      // this unit's tiles: [tb, tb + ntiles) of the row's valid ones
+      const int tb = MODE == 1 ? split * row_nt / n_splits : ta;
+      const int ntiles = MODE == 1 ? (split + 1) * row_nt / n_splits - tb : max(0, min(tb_nom, row_nt) - ta);
       bool fail = *abort != 0;
       if (warp == kFirstProducerWarp && lane == 0 && !fail) {
         if (mbar_wait(&sm.tok_empty[n & 1], ((n >> 1) & 1) ^ 1, A.err, abort)) {
           sm.ntiles[n & 1] = ntiles;
-          if (SPLIT) sm.tbeg[n & 1] = tb;
+          if (MODE != 0) sm.tbeg[n & 1] = tb;
           mbar_arrive(&sm.tok_full[n & 1]);
         } else {
           fail = true;
@@ -582,8 +619,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mma_commit(&sm.s_full[b1]);
       };
-      const int n_units = A.n_rows * (SPLIT ? A.n_splits : 1);
-      for (int u = blockIdx.x; u < n_units && !*abort; u += gridDim.x, ++n) {
+      int tr, split, ta, tb_nom, slot;
+      for (int ui = 0; !*abort && unit_at<MODE>(A, ui, tr, split, ta, tb_nom, slot); ++ui, ++n) {
         if (!mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort)) break;
         const int ntiles = sm.ntiles[n & 1];
         mbar_arrive(&sm.tok_empty[n & 1]);
@@ -658,20 +695,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     // As in the producers, a failed wait skips nothing: the thread finishes the tile (what it
     // computes is discarded) and the failure is ORed into the next group barrier, so that the
     // eight warps leave together.
-    const int n_splits = SPLIT ? A.n_splits : 1;
-    const int n_units = A.n_rows * n_splits;
-    constexpr bool partial = SPLIT;
-    for (int u = blockIdx.x; u < n_units; u += gridDim.x, ++n) {
-      const int tr = u / n_splits, split = u % n_splits;
+    int tr, split, ta, tb_nom, slot;
+    for (int ui = 0; unit_at<MODE>(A, ui, tr, split, ta, tb_nom, slot); ++ui, ++n) {
       const int t = A.tok_begin + tr;
+      const bool partial = MODE != 0 && slot >= 0;  // unit-uniform
       const bool go = *abort == 0 && mbar_wait(&sm.tok_full[n & 1], (n >> 1) & 1, A.err, abort);
       if (bar_red_or(1, kSoftmaxThreads, !go)) break;
       const int ntiles = sm.ntiles[n & 1];
-      const int tb = SPLIT ? sm.tbeg[n & 1] : 0;
+      const int tb = MODE != 0 ? sm.tbeg[n & 1] : 0;
       __syncwarp();
       if (lane == 0) mbar_arrive(&sm.tok_empty[n & 1]);
-      // destination of this unit: the row's output, or its split's partial
-      const int64_t prow = static_cast<int64_t>(split) * A.n_rows + tr;
+      // destination of this unit: the row's output, or its partial slot
+      const int64_t prow = slot;
       __nv_bfloat16* out_row = A.out + static_cast<int64_t>(t) * A.n_heads * DL;
       float* part_row = partial ? A.part_out + prow * A.n_heads * DL : nullptr;
       float* lse_row = partial ? A.part_lse + prow * A.n_heads : A.lse + static_cast<int64_t>(t) * A.n_heads;
@@ -880,6 +915,55 @@ __global__ void split_merge_kernel(const float* __restrict__ parts, const float*
   if (lane == 0) lse[row] = z > 0.f ? mx + logf(z) : -INFINITY;
 }
 
+// Merge of the rows that balanced units split between neighbouring CTAs: the range of CTA cb
+// (cb = 1 .. G - 1) starts at nominal tile g; if g falls inside row r, that row's first part is
+// slot 2 cb - 1 (CTA cb - 1's last unit) and its second part slot 2 cb (CTA cb's first unit).
+// lse = ln(e^lse_a + e^lse_b), out = e^(lse_a - lse) out_a + e^(lse_b - lse) out_b, in fp32.
+// One block per (boundary, 8 heads), one warp per head; every load of a warp is issued before
+// the first is used (the merge is latency-bound otherwise).
+template <int D>
+__global__ void __launch_bounds__(256) balanced_merge_kernel(const float* __restrict__ parts,
+                                                              const float* __restrict__ parts_lse, int G, int n_rows,
+                                                              int T, int n_heads, __nv_bfloat16* __restrict__ out,
+                                                              float* __restrict__ lse) {
+  const int cb = static_cast<int>(blockIdx.x) + 1;
+  const int64_t tot = static_cast<int64_t>(n_rows) * T;
+  const int64_t g = cb * tot / G;
+  if (g % T == 0) return;  // the boundary falls between rows: nothing to merge
+  const int64_t r = g / T;
+  const int lane = threadIdx.x & 31;
+  const int h = static_cast<int>(blockIdx.y) * 8 + (threadIdx.x >> 5);
+  if (h >= n_heads) return;
+  const int64_t sa = 2 * cb - 1, sb = 2 * cb;
+  constexpr int kIt = (D + 127) / 128;  // float4 steps per lane
+  const float* pa = parts + (sa * n_heads + h) * D;
+  const float* pb = parts + (sb * n_heads + h) * D;
+  float4 a[kIt], b[kIt];
+#pragma unroll
+  for (int i = 0; i < kIt; ++i) {
+    const int d0 = 4 * lane + 128 * i;
+    a[i] = d0 < D ? __ldg(reinterpret_cast<const float4*>(pa + d0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+    b[i] = d0 < D ? __ldg(reinterpret_cast<const float4*>(pb + d0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  const float la = __ldg(parts_lse + sa * n_heads + h), lb = __ldg(parts_lse + sb * n_heads + h);
+  const float mx = fmaxf(la, lb);
+  const float wa = (mx == -INFINITY || la == -INFINITY) ? 0.f : expf(la - mx);
+  const float wb = (mx == -INFINITY || lb == -INFINITY) ? 0.f : expf(lb - mx);
+  const float z = wa + wb;
+  const float inv_z = z > 0.f ? 1.f / z : 0.f;
+  const float ca = wa * inv_z, cbw = wb * inv_z;
+  __nv_bfloat16* o = out + (r * n_heads + h) * D;
+#pragma unroll
+  for (int i = 0; i < kIt; ++i) {
+    const int d0 = 4 * lane + 128 * i;
+    if (d0 < D)
+      *reinterpret_cast<uint2*>(o + d0) =
+          make_uint2(pack_bf16x2(ca * a[i].x + cbw * b[i].x, ca * a[i].y + cbw * b[i].y),
+                     pack_bf16x2(ca * a[i].z + cbw * b[i].z, ca * a[i].w + cbw * b[i].w));
+  }
+  if (lane == 0) lse[r * n_heads + h] = z > 0.f ? mx + logf(z) : -INFINITY;
+}
+
 template <int NCH, bool WR>
 smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
   const size_t smem = sizeof(AttnSmem<NCH>) + 1024;
@@ -887,19 +971,21 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
   const int dev = current_device_index();
   if (dev < 0) return SMLA_ERR_CUDA;
   if (!attr_set[dev].load(std::memory_order_acquire)) {
-    if (cudaFuncSetAttribute(attend_kernel<NCH, WR, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(attend_kernel<NCH, WR, 0>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess ||
-        cudaFuncSetAttribute(attend_kernel<NCH, WR, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(attend_kernel<NCH, WR, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(smem)) != cudaSuccess ||
+        cudaFuncSetAttribute(attend_kernel<NCH, WR, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(smem)) != cudaSuccess)
       return SMLA_ERR_CUDA;
     // setmaxnreg.inc can only draw on the registers the CTA was launched with;
     // refuse to launch if the compiled allocation does not cover the split.
-    cudaFuncAttributes fa;
-    cudaFuncAttributes fs;
-    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH, WR, false>) != cudaSuccess ||
-        cudaFuncGetAttributes(&fs, attend_kernel<NCH, WR, true>) != cudaSuccess)
+    cudaFuncAttributes fa, fs, fb;
+    if (cudaFuncGetAttributes(&fa, attend_kernel<NCH, WR, 0>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fs, attend_kernel<NCH, WR, 1>) != cudaSuccess ||
+        cudaFuncGetAttributes(&fb, attend_kernel<NCH, WR, 2>) != cudaSuccess)
       return SMLA_ERR_CUDA;
-    if (fa.numRegs < kLaunchRegs || fs.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
+    if (fa.numRegs < kLaunchRegs || fs.numRegs < kLaunchRegs || fb.numRegs < kLaunchRegs) return SMLA_ERR_UNSUPPORTED;
     attr_set[dev].store(true, std::memory_order_release);
   }
   // Query tiles by tensor-map copies when they match the shared-memory tile exactly: 64 heads,
@@ -928,13 +1014,23 @@ smla_status_t launch_nch(AttnArgs A, cudaStream_t stream) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS)
       A.q_tma = 1;
   }
-  const int grid = min(A.n_rows * A.n_splits, device_sm_count());
-  if (A.n_splits > 1)
-    attend_kernel<NCH, WR, true><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
+  const int sms = device_sm_count();
+  const int grid = A.mode == 2 ? sms : min(A.n_rows * A.n_splits, sms);
+  if (A.mode == 1)
+    attend_kernel<NCH, WR, 1><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
+  else if (A.mode == 2)
+    attend_kernel<NCH, WR, 2><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
   else
-    attend_kernel<NCH, WR, false><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
+    attend_kernel<NCH, WR, 0><<<grid, kThreads, smem, stream>>>(A, q_map, qpe_map);
   if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
-  if (A.n_splits > 1) {
+  if (A.mode == 2) {
+    balanced_merge_kernel<(NCH - 1) * 64><<<dim3(grid - 1, (A.n_heads + 7) / 8), 256, 0, stream>>>(
+        A.part_out, A.part_lse, grid, A.n_rows, A.row_tiles_nom, A.n_heads,
+        A.out + static_cast<int64_t>(A.tok_begin) * A.n_heads * (NCH - 1) * 64,
+        A.lse + static_cast<int64_t>(A.tok_begin) * A.n_heads);
+    if (cudaGetLastError() != cudaSuccess) return SMLA_ERR_CUDA;
+  }
+  if (A.mode == 1) {
     const int64_t rows = static_cast<int64_t>(A.n_rows) * A.n_heads;
     constexpr int kMergeWarps = 8;
     split_merge_kernel<<<static_cast<unsigned>((rows + kMergeWarps - 1) / kMergeWarps), 32 * kMergeWarps, 0, stream>>>(
@@ -971,6 +1067,16 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
     n_splits = min(sms / n_rows, row_tiles_max);
     while (n_splits > 1 && attend_split_bytes(n_heads, L.d_latent, n_rows * n_splits) > split_ws_bytes) --n_splits;
   }
+  // More rows than SMs, with a last round of rows that would leave most SMs idle (at most half of
+  // them busy): every CTA takes the same number of tiles instead (balanced units), and rows that
+  // straddle two CTAs are merged by their lse.  With a fuller last round the one-row-per-CTA
+  // schedule is kept: the gathers of all SMs together are bound by the memory system, so a CTA's
+  // tiles run faster while fewer SMs are busy (measured: 256 rows on 152 SMs, 0.243 ms plain
+  // against 0.262 ms balanced).
+  const int rem = n_rows % sms;
+  const bool balanced = split_ws != nullptr && n_rows > sms && n_rows < 8 * sms && rem != 0 && rem <= sms / 2 &&
+                        row_tiles_max > 1 && attend_split_bytes(n_heads, L.d_latent, 2 * sms) <= split_ws_bytes;
+  const int parts = n_splits > 1 ? n_rows * n_splits : (balanced ? 2 * sms : 0);
   AttnArgs A;
   A.L = L;
   A.n_heads = n_heads;
@@ -995,10 +1101,12 @@ smla_status_t launch_attend(const KernelLayout& L, int n_heads, int top_k, float
   A.host_block_map = host_block_map;
   A.n_host_blocks = n_host_blocks;
   A.n_splits = n_splits;
-  A.part_out = n_splits > 1 ? static_cast<float*>(split_ws) : nullptr;
-  A.part_lse = n_splits > 1 ? reinterpret_cast<float*>(static_cast<uint8_t*>(split_ws) +
-                                                         split_out_bytes(n_heads, L.d_latent, n_rows * n_splits))
-                            : nullptr;
+  A.mode = n_splits > 1 ? 1 : (balanced ? 2 : 0);
+  A.row_tiles_nom = row_tiles_max;
+  A.part_out = parts > 0 ? static_cast<float*>(split_ws) : nullptr;
+  A.part_lse = parts > 0 ? reinterpret_cast<float*>(static_cast<uint8_t*>(split_ws) +
+                                                    split_out_bytes(n_heads, L.d_latent, parts))
+                         : nullptr;
   switch (L.d_latent / 64) {
     case 1: return launch_nch<2, false>(A, stream);
     case 8: {

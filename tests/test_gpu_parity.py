@@ -274,6 +274,39 @@ def test_split_attention_matches_oracle_and_one_cta_path(lens):
     assert np.abs(o - res["out"]).max() <= 1e-2
 
 
+@pytest.mark.parametrize("n_rows", [160, 200])
+def test_balanced_attention_matches_oracle_and_one_cta_path(n_rows):
+    """More rows than SMs with a short last round (on 152 SMs: 8 or 48 rows): with a scratch every
+    CTA takes the same number of tiles, a row that straddles two CTAs is finished from two partials
+    merged by their lse.  Ragged rows (contexts below k leave empty tiles, and some parts empty) must match the
+    oracle, and the one-CTA-per-row path within the attention tolerance."""
+    rng = np.random.default_rng(95 + n_rows)
+    lens = rng.choice([1, 7, 100, 1500, 2048, 2049, 3000, 6000, 9000], size=n_rows).tolist()
+    wl = build_workload("bal", FULL, lens, [1] * n_rows, seed=96, slack_blocks=2)
+    ref = oracle_step(wl, oracle_pool(wl))
+    g = G.cuda_wl(build_workload("bal", FULL, lens, [1] * n_rows, seed=96, slack_blocks=2))
+    lay, prm = G.gpu_layout(g), G.gpu_params(g)
+    pool = G.gpu_pool(g, lay)
+    res = G.run_stages(g, pool, lay, prm, split=False)      # one CTA per row (no scratch)
+    assert res["err"] == 0
+    T, d = g.n_tokens, g.dims
+    topk = torch.as_tensor(res["topk"], device="cuda")
+    ws = torch.empty(smla.attend_workspace_size(lay, prm, T), dtype=torch.uint8, device="cuda")
+    assert ws.numel() > 0
+    out = torch.empty((T, d.n_heads, d.d_latent), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((T, d.n_heads), dtype=torch.float32, device="cuda")
+    smla.smla_attend(lay, prm, pool, 0, g.q, g.q_pe, topk, g.block_table, g.query_start_loc, out, lse, workspace=ws)
+    assert smla.smla_get_last_error() == 0
+    o, l = out.float().cpu().numpy(), lse.cpu().numpy()
+    for t in range(T):
+        assert np.array_equal(res["topk"][t], ref[t]["topk"]), f"topk row {t}"
+    out_ref = np.stack([ref[t]["out"] for t in range(T)])
+    lse_ref = np.stack([ref[t]["lse"] for t in range(T)])
+    G.assert_attention_close(o, l, out_ref, lse_ref, "balanced")
+    assert np.abs(l - res["lse"]).max() <= 1e-3
+    assert np.abs(o - res["out"]).max() <= 1e-2
+
+
 @pytest.mark.parametrize("lens", [[140000, 61000, 30000, 9000], [300000], [200000, 150000, 5000, 1, 3000]])
 def test_topk_rows_split_into_segments(lens):
     """Few long rows and a scratch: each row's segments are selected on their own CTAs and the
