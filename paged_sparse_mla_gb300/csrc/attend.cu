@@ -855,10 +855,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld32(tmem_o + lane_base + d2 * kHeads + 32 * hh, o);
         tmem_ld_wait(o);
         if (d < DL && !partial) {
+          // Lane l holds dim d for 32 heads.  Four heads at a time, a 4x4 transpose within each
+          // group of four lanes gives lane 4g + i head i's four consecutive dims of the group, which
+          // go out as one 8-byte store (instead of four 2-byte ones).  d < DL is warp-uniform.
+          const int i4 = lane & 3;
+          const int dg = d - i4;  // first dim of this lane's group
 #pragma unroll
-          for (int x = 0; x < 32; ++x) {
-            const int h = 32 * hh + x;
-            if (h < A.n_heads) out_row[h * DL + d] = __float2bfloat16(__uint_as_float(o[x]) * sm.l_fin[h]);
+          for (int x0 = 0; x0 < 32; x0 += 4) {
+            float a[4];
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) a[jj] = __uint_as_float(o[x0 + jj]) * sm.l_fin[32 * hh + x0 + jj];
+#pragma unroll
+            for (int st = 2; st >= 1; st >>= 1) {
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                if ((jj & st) == 0) {
+                  const bool hi = (i4 & st) != 0;
+                  const float recv = __shfl_xor_sync(0xffffffffu, hi ? a[jj] : a[jj | st], st);
+                  if (hi) a[jj] = recv;
+                  else a[jj | st] = recv;
+                }
+              }
+            }
+            // a[jj] = head (x0 + i4) at dim dg + jj
+            const int h = 32 * hh + x0 + i4;
+            if (h < A.n_heads)
+              *reinterpret_cast<uint2*>(out_row + h * DL + dg) = make_uint2(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]));
           }
         } else if (d < DL) {
 #pragma unroll
