@@ -227,7 +227,11 @@ size_t smla_topk_workspace_size(const smla_params_t* params, int n_tokens);
  *     selected positions are split into contiguous ranges over several CTAs (one wave in
  *     all); every range yields a normalised fp32 partial output and its lse in the scratch,
  *     and a merge kernel combines them as lse = ln sum_r exp(lse_r),
- *     out = sum_r exp(lse_r - lse) out_r.  Without it, each token runs on one CTA.
+ *     out = sum_r exp(lse_r - lse) out_r.  With more tokens than SMs but a last round that
+ *     would keep at most half of the SMs busy (e.g. 160 tokens on 152 SMs), every CTA takes
+ *     an equal share of all tokens' position tiles instead; a token whose tiles straddle two
+ *     CTAs is merged the same way from two partials.  Without a scratch, each token runs on
+ *     one CTA.  The result agrees with the one-CTA path within rounding.
  */
 smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* params, const void* pool,
                           int layer, const void* q, const void* q_pe, const int32_t* topk_idx,
@@ -235,7 +239,8 @@ smla_status_t smla_attend(const smla_layout_t* layout, const smla_params_t* para
                           int batch, int n_tokens, void* out, float* lse, void* workspace,
                           size_t workspace_bytes, void* stream);
 
-/* Scratch bytes with which smla_attend splits the tokens' ranges over CTAs (0 when
+/* Scratch bytes with which smla_attend splits or balances the tokens' ranges over CTAs:
+ * partial outputs for up to 512 ranges, about 64 MiB for 64 heads of 512 dims (0 when
  * n_tokens is too large to need it). */
 size_t smla_attend_workspace_size(const smla_layout_t* layout, const smla_params_t* params, int n_tokens);
 
