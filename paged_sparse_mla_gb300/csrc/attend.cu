@@ -300,8 +300,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     attend_kernel(const AttnArgs A, const __grid_constant__ CUtensorMap q_map,
                   const __grid_constant__ CUtensorMap qpe_map) {
   extern __shared__ uint8_t smem_raw[];
-  AttnSmem<NCH>& sm =
-      *reinterpret_cast<AttnSmem<NCH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  // 1024-aligned base, formed by pointer arithmetic on the shared array so that accesses stay shared-space
+  AttnSmem<NCH>& sm = *reinterpret_cast<AttnSmem<NCH>*>(
+      smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u));
   constexpr int kLatChunks = NCH - 1;
   constexpr int kChunkBytes = kTile * 128;
   const int warp = threadIdx.x >> 5;

@@ -212,21 +212,23 @@ __device__ void build_item_table(const IdxArgs& A, IdxSmem& sm) {
   if (lane == 31) sm.item_off[A.batch] = incl;
 }
 
-// Four heads of one key: acc0 += ReLU(v0, v1) * w01 and acc1 += (v2 + |v2|, v3 + |v3|) * w23,
-// with packed fp32 pairs.  The second pair carries twice the ReLU-weighted sum (exactly: a
-// factor of two commutes with rounding), which moves half of the ReLUs from the integer/
-// compare pipe onto the FMA pipe; the caller halves acc1's total.
+// Four heads of one key: acc0 += (v0 + |v0|, v1 + |v1|) * w01 and acc1 += (v2 + |v2|, v3 + |v3|) * w23,
+// with packed fp32 pairs.  v + |v| is exactly 2 ReLU(v), so both accumulators carry twice the
+// ReLU-weighted sum (a factor of two commutes with rounding) and the caller halves the total.
+// Each ReLU pair is one packed add whose second operand is the pair's absolute value.
 __device__ __forceinline__ void relu_fma4(uint64_t& acc0, uint64_t& acc1, uint32_t v0, uint32_t v1, uint32_t v2,
                                           uint32_t v3, uint64_t w01, uint64_t w23) {
-  asm("{\n\t.reg .f32 a0, a1, b0, b1;\n\t.reg .b64 p, q;\n\t"
-      "max.f32 a0, %2, 0f00000000;\n\t"
-      "max.f32 a1, %3, 0f00000000;\n\t"
+  asm("{\n\t.reg .f32 a0, a1, b0, b1;\n\t.reg .b64 p, q, pa, qa;\n\t"
+      "abs.f32 a0, %2;\n\t"
+      "abs.f32 a1, %3;\n\t"
       "abs.f32 b0, %4;\n\t"
       "abs.f32 b1, %5;\n\t"
-      "add.rn.f32 b0, b0, %4;\n\t"
-      "add.rn.f32 b1, b1, %5;\n\t"
-      "mov.b64 p, {a0, a1};\n\t"
-      "mov.b64 q, {b0, b1};\n\t"
+      "mov.b64 p, {%2, %3};\n\t"
+      "mov.b64 q, {%4, %5};\n\t"
+      "mov.b64 pa, {a0, a1};\n\t"
+      "mov.b64 qa, {b0, b1};\n\t"
+      "add.rn.f32x2 p, p, pa;\n\t"
+      "add.rn.f32x2 q, q, qa;\n\t"
       "fma.rn.f32x2 %0, p, %6, %0;\n\t"
       "fma.rn.f32x2 %1, q, %7, %1;\n\t}"
       : "+l"(acc0), "+l"(acc1)
@@ -247,8 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     index_scores_kernel(const IdxArgs A, const __grid_constant__ CUtensorMap key_map,
                         const __grid_constant__ CUtensorMap q_map) {
   extern __shared__ uint8_t smem_raw[];
-  IdxSmem& sm = *reinterpret_cast<IdxSmem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int warp = threadIdx.x >> 5;
+  // 1024-aligned base, formed by pointer arithmetic on the shared array so that accesses stay shared-space
+  IdxSmem& sm = *reinterpret_cast<IdxSmem*>(
+      smem_raw + ((1024u - (static_cast<uint32_t>(__cvta_generic_to_shared(smem_raw)) & 1023u)) & 1023u));
+  // warp index broadcast from lane 0: the compiler then treats it (and the roles, TMEM addresses
+  // and branches derived from it) as warp-uniform
+  const int warp = __shfl_sync(0xffffffffu, static_cast<int>(threadIdx.x >> 5), 0);
   const int lane = threadIdx.x & 31;
   constexpr int H = kH;
   constexpr int kBlocks = kTile / kBS;  // blocks per tile
@@ -473,7 +479,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int st = a % kStages;  // the MMA consumed global tile a from stage a % kStages
         const float s_key = sm.kscale[st][row];
         if (mine) {
-          // head h goes to element h % 2 of acc0 (h % 4 < 2) or of acc1 (h % 4 >= 2, doubled)
+          // head h goes to element h % 2 of acc0 (h % 4 < 2) or of acc1 (h % 4 >= 2); every term doubled
           // 16-column TMEM loads, the next one in flight while the current one is reduced
           uint64_t acc0 = 0, acc1 = 0;
           const uint32_t tbase = tmem + lane_base + ab * 256 + tok * H;
@@ -490,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         wp[(c * 16 + x) / 2], wp[(c * 16 + x) / 2 + 1]);
             if (more) tmem_ld_wait(v[(c + 1) & 1]);
           }
-          const float total = pair_sum(acc0) + 0.5f * pair_sum(acc1);
+          const float total = 0.5f * (pair_sum(acc0) + pair_sum(acc1));
           if (j < j_end) srow[j] = total * s_key;
         }
         tc_fence_before();
