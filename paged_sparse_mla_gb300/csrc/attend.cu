@@ -255,6 +255,18 @@ __device__ __forceinline__ void load_units(const uint8_t* const* rec, int u0, in
   }
 }
 
+// (a.x * s, a.y * s) with one packed fp32 multiply (each product rounded as by a scalar multiply).
+__device__ __forceinline__ float2 mul2(float2 a, float s) {
+  uint64_t r;
+  asm("{\n\t.reg .b64 x, y;\n\t"
+      "mov.b64 x, {%1, %2};\n\t"
+      "mov.b64 y, {%3, %3};\n\t"
+      "mul.rn.f32x2 %0, x, y;\n\t}"
+      : "=l"(r)
+      : "f"(a.x), "f"(a.y), "f"(s));
+  return make_float2(__uint_as_float(static_cast<uint32_t>(r)), __uint_as_float(static_cast<uint32_t>(r >> 32)));
+}
+
 // 16 E4M3 codes (little-endian in `codes`) times `sc` -> 16 bf16 in two 16-byte words.
 __device__ __forceinline__ void dequant16(const uint4& codes, float sc, uint4& o0, uint4& o1) {
   const uint32_t cw[4] = {codes.x, codes.y, codes.z, codes.w};
@@ -265,8 +277,9 @@ __device__ __forceinline__ void dequant16(const uint4& codes, float sc, uint4& o
     const __half2_raw h23 = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(cw[x] >> 16), __NV_E4M3);
     const float2 f01 = __half22float2(*reinterpret_cast<const __half2*>(&h01));
     const float2 f23 = __half22float2(*reinterpret_cast<const __half2*>(&h23));
-    ow[2 * x] = pack_bf16x2(f01.x * sc, f01.y * sc);
-    ow[2 * x + 1] = pack_bf16x2(f23.x * sc, f23.y * sc);
+    const float2 p01 = mul2(f01, sc), p23 = mul2(f23, sc);
+    ow[2 * x] = pack_bf16x2(p01.x, p01.y);
+    ow[2 * x + 1] = pack_bf16x2(p23.x, p23.y);
   }
   o0 = make_uint4(ow[0], ow[1], ow[2], ow[3]);
   o1 = make_uint4(ow[4], ow[5], ow[6], ow[7]);
