@@ -92,11 +92,7 @@ __device__ __forceinline__ void add_to_hist(int* hist, uint32_t key, bool in_row
                                             int shift, uint32_t bmask) {
   const bool hit = in_row && (key & mask) == prefix;
   const uint32_t bin = (key >> shift) & bmask;
-  const uint32_t active = __ballot_sync(0xffffffffu, hit);
-  if (hit) {
-    const uint32_t peers = __match_any_sync(active, bin);
-    if ((threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
-  }
+  if (hit) atomicAdd(&hist[bin], 1);
 }
 
 // Visit every element of the row (float4 loads when the row is 16-byte aligned).
@@ -447,8 +443,13 @@ __device__ void topk_core(TopkSmem& sm, const float* __restrict__ s, int n, int 
 #pragma unroll 4
     for (int i = threadIdx.x; i < runs; i += kThreads) {
       const int j = static_cast<int>((static_cast<int64_t>(i) * (n - 4)) / (runs - 1));
+      if (aligned) {  // the run starts on a 16-byte boundary: one vector load
+        const float4 v = __ldg(reinterpret_cast<const float4*>(s + (j & ~3)));
+        *reinterpret_cast<uint4*>(samp + 4 * i) = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+      } else {
 #pragma unroll
-      for (int x = 0; x < 4; ++x) samp[4 * i + x] = order_key(__ldg(s + j + x));
+        for (int x = 0; x < 4; ++x) samp[4 * i + x] = order_key(__ldg(s + j + x));
+      }
     }
     // rank of the threshold in the sample: expected rank of the k-th largest plus a margin
     const int r = static_cast<int>((static_cast<int64_t>(k) * kSample + n - 1) / n);
