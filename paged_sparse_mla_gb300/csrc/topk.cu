@@ -40,7 +40,7 @@ constexpr int kSample = 8192;  // sample size for the threshold (runs of 4)
 constexpr int kMaxK = 4096;    // largest k of the fast path (power of two)
 constexpr int kWarpCap = kCap / kWarps;  // candidates per warp list (512)
 constexpr int kSpan = 32 * 16;           // positions a warp scans per iteration (16 per lane)
-constexpr int kPrefetchAhead = 4096;     // positions each warp keeps requested into L2 ahead of its scan
+constexpr int kPrefetchAhead = 1024;     // positions each warp keeps requested into L2 ahead of its scan
 
 struct TopkSmem {
   int hist[kBins];
