@@ -19,11 +19,14 @@
 //     M = 64 keys, N = 64 heads, fp32 in tensor memory, two buffers.  Key i of
 //     the tile sits in TMEM lane (i % 16) + 32 (i / 16).
 //   * Softmax (warps 0-7; warp w holds keys 16 (w % 4) .. + 15 and heads
-//     32 (w / 4) .. + 31): per-head tile maxima with a butterfly
-//     transpose-reduction across lanes, online softmax with lazy rescaling
-//     (the running max only moves when a head's tile max exceeds it by 2^8),
-//     P^T[key, head] written as bf16 into the rope chunk (free after MMA1),
-//     per-thread partial row sums.
+//     32 (w / 4) .. + 31): the 16x32bx2 tensor-memory load gives lane l of the
+//     warp key l % 16 and 16 of the 32 heads (half l / 16), so every lane has
+//     scores (the other 16 lanes of each TMEM sub-partition hold none);
+//     per-head tile maxima by shuffles within each half-warp, online softmax
+//     with lazy rescaling (the running max only moves when a head's tile max
+//     exceeds it by 2^8), P^T[key, head] written as bf16 into the rope chunk
+//     (free after MMA1), per-thread partial row sums reduced within the
+//     half-warps at the end of the token.
 //   * MMA2: O^T[dim, head] += V^T[dim, key] . P^T[key, head] with both operands
 //     MN-major: the same swizzled latent chunks serve as V^T without a
 //     transpose; M = 128 dims x 4 tiles, N = 64 heads, K = 64 keys.  The MMA
@@ -146,23 +149,31 @@ __device__ __forceinline__ bool unit_at(const AttnArgs& A, int i, int& tr, int& 
   }
 }
 
-// Transpose-reduce 32 per-lane values across the 32 lanes of a warp: afterwards
-// lane l holds the reduction of value l in v[0].
-template <bool kMax>
-__device__ __forceinline__ void warp_transpose_reduce32(float (&v)[32], int lane) {
+// Within each half-warp: lane 16 u + l holds, in v[0], the sum over the half's 16 lanes of value l.
+__device__ __forceinline__ void half_transpose_sum16(float (&v)[16], int lane) {
 #pragma unroll
-  for (int st = 0; st < 5; ++st) {
-    const int off = 16 >> st;
-    const int half = 16 >> st;
+  for (int st = 0; st < 4; ++st) {
+    const int off = 8 >> st;
     const bool upper = (lane & off) != 0;
 #pragma unroll
-    for (int i = 0; i < half; ++i) {
-      const float send = upper ? v[i] : v[i + half];
-      const float keep = upper ? v[i + half] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-      v[i] = kMax ? fmaxf(keep, recv) : keep + recv;
+    for (int i = 0; i < off; ++i) {
+      const float send = upper ? v[i] : v[i + off];
+      const float keep = upper ? v[i + off] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
     }
   }
+}
+
+// tcgen05.ld 16x32bx2: 16 TMEM lanes read twice, the second time `kSplit` columns further on;
+// thread t holds lane t % 16, columns (t / 16) * kSplit + 0 .. 15.
+template <int kSplit>
+__device__ __forceinline__ void tmem_ld16x32bx2_x16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr), "n"(kSplit));
 }
 
 // Non-blocking test of the phase of `bar` with the given parity.
@@ -175,13 +186,6 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "r"(smem_u32(bar)), "r"(parity)
       : "memory");
   return ok != 0;
-}
-
-// Maximum of v over the 32 lanes (every lane receives it).
-__device__ __forceinline__ float warp_max(float v) {
-  float r;
-  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
-  return r;
 }
 
 // 2^x with the hardware approximation (MUFU; relative error ~2^-22, -inf -> 0).
@@ -703,7 +707,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;            // 0..255
     const int sp = warp & 3;                // TMEM sub-partition
     const int hh = warp >> 2;               // head half: heads 32 hh .. 32 hh + 31
-    const int key = 16 * sp + lane;         // key of the tile (lanes < 16)
+    const int key = 16 * sp + (lane & 15);  // key of the tile (S^T rows sit in TMEM lanes 0-15 of a sub-partition)
+    const int hs = lane >> 4;               // this thread's heads: 32 hh + 16 hs .. + 15
     const uint32_t lane_base = static_cast<uint32_t>(sp * 32) << 16;
     uint32_t n = 0, nw = 0, kk = 0;
     // As in the producers, a failed wait skips nothing: the thread finishes the tile (what it
@@ -733,23 +738,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         continue;
       }
       const int32_t* idx = A.topk + static_cast<int64_t>(tr) * A.top_k;
-      float l_part[32];
+      float l_part[16];
 #pragma unroll
-      for (int h = 0; h < 32; ++h) l_part[h] = 0.f;
+      for (int h = 0; h < 16; ++h) l_part[h] = 0.f;
       bool ok = true, failed = false;
       for (int tile = 0; tile < ntiles; ++tile, ++kk) {
         const int kb = kk & 1;
         const int e = (tb + tile) * kTile + key;
-        const bool valid = lane < 16 && e < A.top_k && __ldg(idx + e) >= 0;
+        const bool valid = e < A.top_k && __ldg(idx + e) >= 0;
         ok = ok && mbar_wait(&sm.s_full[kb], (kk >> 1) & 1, A.err, abort);
         tc_fence_after();
-        float sc[32];
+        float sc[16];
         {
-          uint32_t r[32];
-          tmem_ld32(tmem_s + lane_base + kb * kHeads + 32 * hh, r);
+          uint32_t r[16];
+          tmem_ld16x32bx2_x16<16>(tmem_s + lane_base + kb * kHeads + 32 * hh, r);
           tmem_ld_wait(r);
 #pragma unroll
-          for (int h = 0; h < 32; ++h) sc[h] = valid ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
+          for (int h = 0; h < 16; ++h) sc[h] = valid ? __uint_as_float(r[h]) * A.scale_log2 : -INFINITY;
         }
         tc_fence_before();
         __syncwarp();
@@ -763,17 +768,19 @@ __global__ void __launch_bounds__(kThreads, 1)
         int exceed = tile == 0 || !ok;
         if (!exceed) {
 #pragma unroll
-          for (int h = 0; h < 32; ++h) exceed |= sc[h] > sm.m_run[32 * hh + h] + kRescaleThreshold;
+          for (int h = 0; h < 16; ++h) exceed |= sc[h] > sm.m_run[32 * hh + 16 * hs + h] + kRescaleThreshold;
         }
         bool moved = false;
         if (bar_red_or(1, kSoftmaxThreads, exceed)) {
-          // per-head maximum of this tile over the warp's keys; lane h keeps head 32 hh + h
+          // per-head maximum of this tile over the warp's 16 keys; lane 16 hs + h keeps head 32 hh + 16 hs + h
           {
             float mine = -INFINITY;
 #pragma unroll
-            for (int h = 0; h < 32; ++h) {
-              const float m = warp_max(sc[h]);
-              mine = lane == h ? m : mine;
+            for (int h = 0; h < 16; ++h) {
+              float m = sc[h];
+#pragma unroll
+              for (int off = 8; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+              mine = (lane & 15) == h ? m : mine;
             }
             sm.red[sp][32 * hh + lane] = mine;
           }
@@ -801,15 +808,15 @@ __global__ void __launch_bounds__(kThreads, 1)
           named_bar_sync(1, kSoftmaxThreads);
           if (tile > 0) {
 #pragma unroll
-            for (int h = 0; h < 32; ++h) l_part[h] *= sm.alpha[32 * hh + h];
+            for (int h = 0; h < 16; ++h) l_part[h] *= sm.alpha[32 * hh + 16 * hs + h];
           }
         }
         // probabilities -> bf16 P^T row (this key, this warp's 32 heads) in the rope chunk
         {
-          uint32_t pw[16];
+          uint32_t pw[8];
 #pragma unroll
-          for (int hx = 0; hx < 32; hx += 2) {
-            const int h = 32 * hh + hx;
+          for (int hx = 0; hx < 16; hx += 2) {
+            const int h = 32 * hh + 16 * hs + hx;
             const float m0 = sm.m_run[h], m1 = sm.m_run[h + 1];
             const float p0 = fast_exp2(sc[hx] - (m0 == -INFINITY ? 0.f : m0));
             const float p1 = fast_exp2(sc[hx + 1] - (m1 == -INFINITY ? 0.f : m1));
@@ -819,12 +826,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             l_part[hx + 1] += pf.y;
             pw[hx / 2] = (static_cast<uint32_t>(__bfloat16_as_ushort(pb.y)) << 16) | __bfloat16_as_ushort(pb.x);
           }
-          if (lane < 16) {
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              *reinterpret_cast<uint4*>(&sm.kv[kb][kLatChunks][sw128_off(key, 4 * hh + v)]) =
-                  make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
-            }
+          for (int v = 0; v < 2; ++v) {
+            *reinterpret_cast<uint4*>(&sm.kv[kb][kLatChunks][sw128_off(key, 4 * hh + 2 * hs + v)]) =
+                make_uint4(pw[4 * v], pw[4 * v + 1], pw[4 * v + 2], pw[4 * v + 3]);
           }
         }
         // rescale O^T when a running max moved; it holds MMA2 of the previous tile once that
@@ -853,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ---- end of token: row sums, normalisation, lse ----
       ok = ok && mbar_wait(&sm.o_done, nw & 1, A.err, abort);
       tc_fence_after();
-      warp_transpose_reduce32<false>(l_part, lane);
+      half_transpose_sum16(l_part, lane);
       sm.red[sp][32 * hh + lane] = l_part[0];
       if (bar_red_or(1, kSoftmaxThreads, !ok)) break;
       if (tid < kHeads) {
