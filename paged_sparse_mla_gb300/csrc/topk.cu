@@ -437,18 +437,19 @@ __device__ void topk_core(TopkSmem& sm, const float* __restrict__ s, int n, int 
   // ---- threshold from a sample (skipped when every position fits) ----
   uint32_t thr = 0;  // keep keys >= thr
   if (n > kCap) {
-    // sample: kSample / 4 runs of 4 consecutive positions, evenly spread over the row
+    // sample: kSample / 32 runs of 32 consecutive positions (a 128-byte line each when the row is
+    // aligned), evenly spread over the row; thread f reads 4 positions of run f / 8
     uint32_t* samp = reinterpret_cast<uint32_t*>(sm.cand);
-    const int runs = kSample / 4;
+    constexpr int runs = kSample / 32;
 #pragma unroll 4
-    for (int i = threadIdx.x; i < runs; i += kThreads) {
-      const int j = static_cast<int>((static_cast<int64_t>(i) * (n - 4)) / (runs - 1));
-      if (aligned) {  // the run starts on a 16-byte boundary: one vector load
-        const float4 v = __ldg(reinterpret_cast<const float4*>(s + (j & ~3)));
-        *reinterpret_cast<uint4*>(samp + 4 * i) = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
+    for (int f = threadIdx.x; f < kSample / 4; f += kThreads) {
+      const int j = static_cast<int>((static_cast<int64_t>(f >> 3) * (n - 32)) / (runs - 1));
+      if (aligned) {  // runs start on a 128-byte boundary of the row: whole-line vector loads
+        const float4 v = __ldg(reinterpret_cast<const float4*>(s + (j & ~31) + 4 * (f & 7)));
+        *reinterpret_cast<uint4*>(samp + 4 * f) = make_uint4(order_key(v.x), order_key(v.y), order_key(v.z), order_key(v.w));
       } else {
 #pragma unroll
-        for (int x = 0; x < 4; ++x) samp[4 * i + x] = order_key(__ldg(s + j + x));
+        for (int x = 0; x < 4; ++x) samp[4 * f + x] = order_key(__ldg(s + j + 4 * (f & 7) + x));
       }
     }
     // rank of the threshold in the sample: expected rank of the k-th largest plus a margin
