@@ -361,7 +361,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         const uint32_t n_have = __popc(__ballot_sync(0xffffffffu, have));
-        if (!mbar_wait(&sm.key_empty[s], ((k / kStages) & 1) ^ 1, A.err, abort)) {
+        // the producer runs up to kStages tiles ahead: its wait for a free stage sleeps between tests
+        if (!mbar_wait_lazy<256>(&sm.key_empty[s], ((k / kStages) & 1) ^ 1, A.err, abort)) {
           ok = false;
           break;
         }
