@@ -235,6 +235,37 @@ __device__ __forceinline__ void relu_fma4(uint64_t& acc0, uint64_t& acc1, uint32
       : "r"(v0), "r"(v1), "r"(v2), "r"(v3), "l"(w01), "l"(w23));
 }
 
+// mbar_wait's bound for a wait that is usually far from complete and off the critical path (a
+// producer several stages ahead of its consumer): a non-blocking test, then a sleep of kSleepNs,
+// so that the waiting warp takes few issue slots from the warps of its SM sub-partition.
+template <uint32_t kSleepNs>
+__device__ __forceinline__ bool mbar_wait_lazy(uint64_t* bar, uint32_t parity, unsigned* err, volatile int* abort) {
+  const uint32_t addr = smem_u32(bar);
+  uint64_t t0 = 0;
+  for (uint32_t i = 0;; ++i) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(addr), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    __nanosleep(kSleepNs);
+    if ((i & 15u) == 15u) {
+      if (*abort) return false;
+      const uint64_t t = globaltimer_ns();
+      if (t0 == 0) {
+        t0 = t;
+      } else if (t - t0 > kWaitLimitNs) {
+        latch_error(err, SMLA_ERR_TIMEOUT);
+        *abort = 1;
+        return false;
+      }
+    }
+  }
+}
+
 __device__ __forceinline__ float pair_sum(uint64_t p) {
   return __uint_as_float(static_cast<uint32_t>(p)) + __uint_as_float(static_cast<uint32_t>(p >> 32));
 }
