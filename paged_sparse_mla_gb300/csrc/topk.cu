@@ -6,14 +6,16 @@
 //
 // One CTA per query row; scores map to order-preserving 32-bit keys (-0 folded
 // onto +0).  Fast path, one coalesced read of the row:
-//   1. an 8,192-element strided sample (runs of 4) is radix-selected (top 24 key
-//      bits) in shared memory to a threshold T whose rank in the sample leaves a
-//      safety margin above k/n of the sample;
+//   1. an 8,192-element sample (256 runs of 32 consecutive positions, whole
+//      128-byte lines of an aligned row, evenly spread) is radix-selected (top 24
+//      key bits) in shared memory to a threshold T whose rank in the sample
+//      leaves a safety margin above k/n of the sample; the radix histograms count
+//      with plain shared-memory atomics;
 //   2. warp w scans its own contiguous segment of the row and appends every
 //      element with key >= T, as a 64-bit (key, ~position) pair, to its own list
 //      in shared memory, in position order (16 keys per lane per iteration, the
 //      next 16 in flight; one warp scan per iteration places the hits).  Bulk
-//      L2 prefetches run 16 KB ahead of each warp.  (Prefetching the start of
+//      L2 prefetches run 4 KB ahead of each warp.  (Prefetching the start of
 //      each segment before the sample was measured: those lines were evicted
 //      before use and read again, +64 MB per launch and slower.)
 // If at least k were collected and no list overflowed, a radix select over the
@@ -36,7 +38,7 @@ constexpr int kThreads = 512;
 constexpr int kWarps = kThreads / 32;
 constexpr int kBins = 4096;
 constexpr int kCap = 8192;     // candidate capacity of the fast path (power of two)
-constexpr int kSample = 8192;  // sample size for the threshold (runs of 4)
+constexpr int kSample = 8192;  // sample size for the threshold (runs of 32)
 constexpr int kMaxK = 4096;    // largest k of the fast path (power of two)
 constexpr int kWarpCap = kCap / kWarps;  // candidates per warp list (512)
 constexpr int kSpan = 32 * 16;           // positions a warp scans per iteration (16 per lane)
